@@ -1,0 +1,184 @@
+"""CPU oracle for per-token-group fp8 e4m3 quantization -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never does, and this package imports nothing from it.
+
+The arithmetic lives in ``gq_oracle.c`` (plain C, compiled with gcc); this
+module compiles it on demand and exposes numpy-level wrappers.  bf16 tensors
+travel as their raw ``uint16`` bit patterns, e4m3 results as ``uint8`` codes.
+
+Method source: pytorch/ao pull-request pages #2668 ("use smaller block sizes
+for per group scaling kernels", intro and the kernel arguments in its
+torch.compile failure report) and #2863 ("test and bench new faster method for
+per group rowwise scaling", Summary).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "gq_oracle.c")
+_LIB = os.path.join(_HERE, "libgq_oracle.so")
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+          "-fno-fast-math", "-Wall", "-Wextra"]
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile an oracle C source file into a shared library at ``out``."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gq_oracle.c`` into ``libgq_oracle.so`` when it is stale."""
+    stale = (not os.path.exists(_LIB)
+             or os.path.getmtime(_LIB) < os.path.getmtime(SOURCE))
+    if force or stale:
+        compile_source(SOURCE, _LIB)
+    return _LIB
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+class Oracle:
+    """numpy-level view of one compiled oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        lib.gqo_colwise.argtypes = [p, i64, i64, p, i32, p, p]
+        lib.gqo_colwise.restype = ctypes.c_int
+        lib.gqo_rowwise_t.argtypes = [p, i64, i64, p, i32, p, p]
+        lib.gqo_rowwise_t.restype = ctypes.c_int
+        lib.gqo_e4m3_encode_array.argtypes = [p, i64, p]
+        lib.gqo_e4m3_decode_array.argtypes = [p, i64, p]
+        lib.gqo_scale_array.argtypes = [p, i64, p]
+        lib.gqo_quant_array.argtypes = [p, p, i64, p]
+        for f in ("gqo_e4m3_encode_array", "gqo_e4m3_decode_array",
+                  "gqo_scale_array", "gqo_quant_array"):
+            getattr(lib, f).restype = None
+        self.lib = lib
+        self.path = path
+
+    # ---------------------------------------------------------- elementwise
+    def e4m3_encode(self, v) -> np.ndarray:
+        """Saturating round-to-nearest-even fp32 -> e4m3 codes (uint8)."""
+        v = _c(v, np.float32)
+        out = np.empty(v.shape, np.uint8)
+        self.lib.gqo_e4m3_encode_array(v.ctypes.data, v.size, out.ctypes.data)
+        return out
+
+    def e4m3_decode(self, codes) -> np.ndarray:
+        """e4m3 codes -> float64 values (NaN for S.1111.111)."""
+        c = _c(codes, np.uint8)
+        out = np.empty(c.shape, np.float64)
+        self.lib.gqo_e4m3_decode_array(c.ctypes.data, c.size, out.ctypes.data)
+        return out
+
+    def scale_of(self, amax) -> np.ndarray:
+        """fp32 scale = 448 / max(amax, 1e-12) for an array of fp32 amax."""
+        a = _c(amax, np.float32)
+        out = np.empty(a.shape, np.float32)
+        self.lib.gqo_scale_array(a.ctypes.data, a.size, out.ctypes.data)
+        return out
+
+    def quant(self, x_bf16_bits, scale) -> np.ndarray:
+        """Elementwise e4m3(fp32(x * scale)); x as bf16 bit patterns."""
+        x = _c(x_bf16_bits, np.uint16)
+        s = _c(np.broadcast_to(np.asarray(scale, np.float32), x.shape),
+               np.float32)
+        out = np.empty(x.shape, np.uint8)
+        self.lib.gqo_quant_array(x.ctypes.data, s.ctypes.data, x.size,
+                                 out.ctypes.data)
+        return out
+
+    # ---------------------------------------------------------------- paths
+    def colwise(self, x_bf16_bits, offs, out=None):
+        """Per-group scaling along dim0.
+
+        x: uint16 (M, K) bf16 bits, row-major.  offs: int32 end offsets.
+        Returns (q uint8 (M, K), scales float32 (n_groups, K)).  Rows outside
+        every group keep the value of ``out`` (zeros when ``out`` is None).
+        """
+        x = _c(x_bf16_bits, np.uint16)
+        assert x.ndim == 2
+        o = _c(offs, np.int32).reshape(-1)
+        M, K = x.shape
+        q = np.zeros((M, K), np.uint8) if out is None else _c(out, np.uint8).copy()
+        s = np.empty((o.size, K), np.float32)
+        rc = self.lib.gqo_colwise(x.ctypes.data, M, K, o.ctypes.data, o.size,
+                                  q.ctypes.data, s.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle colwise: invalid arguments")
+        return q, s
+
+    def rowwise_t(self, a_bf16_bits, offs, out=None):
+        """Per-group scaling along dim1 with transposed output.
+
+        a: uint16 (N, Mg) bf16 bits, row-major.  offs: int32 end offsets
+        along Mg.  Returns (qt uint8 (Mg, N) = q(a)^T, scales float32
+        (N, n_groups)).  Token rows of qt outside every group keep ``out``.
+        """
+        a = _c(a_bf16_bits, np.uint16)
+        assert a.ndim == 2
+        o = _c(offs, np.int32).reshape(-1)
+        N, Mg = a.shape
+        qt = np.zeros((Mg, N), np.uint8) if out is None else _c(out, np.uint8).copy()
+        s = np.empty((N, o.size), np.float32)
+        rc = self.lib.gqo_rowwise_t(a.ctypes.data, N, Mg, o.ctypes.data,
+                                    o.size, qt.ctypes.data, s.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle rowwise_t: invalid arguments")
+        return qt, s
+
+
+_lock = threading.Lock()
+_default: Oracle | None = None
+
+
+def get() -> Oracle:
+    """The oracle built from ``gq_oracle.c``."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default
+
+
+def e4m3_encode(v):
+    return get().e4m3_encode(v)
+
+
+def e4m3_decode(codes):
+    return get().e4m3_decode(codes)
+
+
+def scale_of(amax):
+    return get().scale_of(amax)
+
+
+def quant(x_bf16_bits, scale):
+    return get().quant(x_bf16_bits, scale)
+
+
+def colwise(x_bf16_bits, offs, out=None):
+    return get().colwise(x_bf16_bits, offs, out)
+
+
+def rowwise_t(a_bf16_bits, offs, out=None):
+    return get().rowwise_t(a_bf16_bits, offs, out)
+
+
+def threads_used() -> int:
+    """The oracle is single-threaded."""
+    return 1

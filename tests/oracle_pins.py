@@ -1,0 +1,306 @@
+"""Pins that tie the CPU oracle to facts outside itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with what the pages, the e4m3 format definition, the
+mathematics or an independent library routine fix.  ``test_oracle_pins.py``
+runs them on the real oracle; ``test_oracle_mutants.py`` runs them on copies
+of the oracle with a planted mistake and requires each copy to fail one.
+"""
+from __future__ import annotations
+
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import ref_loop
+from fp8_quantization_moe_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _f32_from_bits(u):
+    return np.asarray(u, np.uint32).view(np.float32)
+
+
+def _torch_e4m3(v):
+    return ref_loop.cast_e4m3(np.asarray(v, np.float32))
+
+
+# ------------------------------------------------------------ the format --
+
+def pin_decode_landmarks(o):
+    """Decode agrees with the OCP E4M3 table's landmark codes."""
+    g = _golden("e4m3_landmarks.json")
+    for code, val in g["codes"].items():
+        got = o.e4m3_decode([int(code, 16)])[0]
+        assert got == val and np.signbit(got) == np.signbit(val), (code, got, val)
+    for code in g["nan_codes"]:
+        assert np.isnan(o.e4m3_decode([int(code, 16)])[0]), code
+
+
+def pin_decode_vs_torch(o):
+    """All 256 codes decode as torch.float8_e4m3fn does."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = o.e4m3_decode(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def pin_encode_roundtrip(o):
+    """encode(decode(c)) == c for every finite code, signed zeros included."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    vals = o.e4m3_decode(codes).astype(np.float32)
+    assert np.array_equal(o.e4m3_encode(vals), codes)
+
+
+def pin_encode_midpoints(o):
+    """Exact midpoints between neighbouring codes go to the even code; one
+    fp32 ulp either side goes to the nearer code."""
+    pos = o.e4m3_decode(np.arange(0, 127, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)
+    for c in range(126):
+        lo, hi = pos[c], pos[c + 1]
+        mid = np.float32((lo + hi) / 2)  # exact: at most 5 significant bits
+        assert float(mid) == (lo + hi) / 2
+        even = c if c % 2 == 0 else c + 1
+        below = np.nextafter(mid, np.float32(0))
+        above = np.nextafter(mid, np.float32(np.inf))
+        got = o.e4m3_encode(np.array([mid, below, above, -mid], np.float32))
+        assert list(got) == [even, c, c + 1, even | 0x80], (c, got)
+
+
+def pin_encode_boundaries(o):
+    """Saturation at +-448 (the pages' fp8_dtype_max / min) and underflow."""
+    k = _golden("pages_constants.json")
+    cases = [
+        (k["fp8_dtype_max"], 0x7E), (k["fp8_dtype_min"], 0xFE),
+        (463.99, 0x7E), (464.0, 0x7E), (480.0, 0x7E), (1e30, 0x7E),
+        (-1e30, 0xFE), (float(np.finfo(np.float32).max), 0x7E),
+        (float("inf"), 0x7E),
+        (2.0 ** -10, 0x00), (-(2.0 ** -10), 0x80), (2.0 ** -12, 0x00),
+        (float(np.nextafter(np.float32(2.0 ** -10), np.float32(1))), 0x01),
+        (0.0, 0x00), (-0.0, 0x80),
+    ]
+    vals = np.array([v for v, _ in cases], np.float32)
+    got = o.e4m3_encode(vals)
+    for (v, want), g in zip(cases, got):
+        assert g == want, (v, hex(g), hex(want))
+    assert o.e4m3_decode([0x7E])[0] == k["fp8_dtype_max"]
+    assert o.e4m3_decode([0xFE])[0] == k["fp8_dtype_min"]
+
+
+def pin_encode_vs_torch(o, exp_lo=116, exp_hi=135, stride=1, neg_stride=97):
+    """Every positive fp32 with biased exponent in [exp_lo, exp_hi] (2^-11 up
+    to 2^9) encodes as torch's RNE cast after clamping; negatives on a strided
+    sample must mirror with the sign bit; below 2^-11 everything is a signed
+    zero and at or above 448 everything saturates."""
+    mant = np.arange(0, 1 << 23, stride, dtype=np.uint32)
+    for e in range(exp_lo, exp_hi + 1):
+        v = _f32_from_bits((np.uint32(e) << 23) | mant)
+        got = o.e4m3_encode(v)
+        ref = _torch_e4m3(v)
+        bad = np.nonzero(got != ref)[0]
+        assert bad.size == 0, (e, v[bad[:4]], got[bad[:4]], ref[bad[:4]])
+        vn = -v[::neg_stride]
+        assert np.array_equal(o.e4m3_encode(vn), ref[::neg_stride] | 0x80), e
+    rng = np.random.default_rng(5)
+    tiny = _f32_from_bits(rng.integers(0, 116 << 23, size=100_000,
+                                       dtype=np.uint32))
+    assert np.all(o.e4m3_encode(tiny) == 0) and np.all(o.e4m3_encode(-tiny) == 0x80)
+    big = _f32_from_bits(rng.integers(0x43E00000, 0x7F800000, size=100_000,
+                                      dtype=np.uint32))
+    assert np.all(o.e4m3_encode(big) == 0x7E) and np.all(o.e4m3_encode(-big) == 0xFE)
+
+
+# ---------------------------------------------------------------- scale --
+
+def _is_rn_f32(s: np.float32, exact: Fraction) -> bool:
+    fs = Fraction(float(s))
+    lo = Fraction(float(np.nextafter(s, np.float32(0))))
+    hi = Fraction(float(np.nextafter(s, np.float32(np.inf))))
+    d, dl, dh = abs(exact - fs), abs(exact - lo), abs(exact - hi)
+    if d < dl and d < dh:
+        return True
+    if d == dl or d == dh:  # a tie: the kept value must have an even mantissa
+        return int(np.float32(s).view(np.uint32)) % 2 == 0
+    return False
+
+
+def pin_scale_exact(o):
+    """For every finite non-negative bf16 amax (|x| of a bf16 is a bf16), the
+    scale is the correctly rounded fp32 of 448 / max(amax, fp32(1e-12)),
+    checked in exact rational arithmetic."""
+    k = _golden("pages_constants.json")
+    bits = np.arange(0, 0x7F80, dtype=np.uint32)  # +0 .. largest finite bf16
+    amax = _f32_from_bits(bits << 16)
+    got = o.scale_of(amax)
+    eps = Fraction(float(np.float32(k["EPS"])))
+    num = Fraction(k["fp8_dtype_max"])
+    for a, s in zip(amax.tolist(), got):
+        d = max(Fraction(a), eps)
+        assert _is_rn_f32(np.float32(s), num / d), (a, s)
+
+
+def pin_quant_single_rounding(o):
+    """q(x, s) = e4m3(RN_fp32(x * s)): the exact product (8 x 24 significant
+    bits fits a double) is rounded once to fp32, then cast by torch.  Half the
+    samples are random; the other half put x * s within a few fp32 ulps of an
+    e4m3 rounding midpoint, where a second rounding or a reassociated product
+    would flip the code."""
+    rng = np.random.default_rng(11)
+    n = 200_000
+    xb = rng.integers(0, 1 << 16, size=n, dtype=np.uint32).astype(np.uint16)
+    xb = xb[((xb & 0x7F80) != 0x7F80) & ((xb & 0x7FFF) > 0x0100)]
+    xf = ref_loop.bf16_bits_to_f32(xb)
+    with np.errstate(over="ignore"):
+        amax = np.abs(xf) * rng.uniform(1.0, 4.0, size=xf.size).astype(np.float32)
+    s_rand = ref_loop.FP8_MAX / np.maximum(amax, ref_loop.EPS)
+    # near-tie samples: target an e4m3 midpoint t, take s = RN(t / x) +- k ulp
+    mags = o.e4m3_decode(np.arange(0, 127, dtype=np.uint8))
+    mids = (mags[:-1] + mags[1:]) / 2
+    t = mids[rng.integers(0, mids.size, size=xf.size)]
+    with np.errstate(over="ignore"):
+        s0 = (t / np.abs(xf.astype(np.float64))).astype(np.float32)
+    k = rng.integers(-3, 4, size=xf.size).astype(np.int32)
+    s_tie = (s0.view(np.int32) + k).view(np.float32)
+    ok = np.isfinite(s_tie) & (s_tie > 0)
+    for xs, ss in ((xb, s_rand), (xb[ok], s_tie[ok])):
+        xs_f = ref_loop.bf16_bits_to_f32(xs).astype(np.float64)
+        v = (xs_f * ss.astype(np.float64)).astype(np.float32)
+        assert np.array_equal(o.quant(xs, ss), _torch_e4m3(v))
+
+
+def pin_hand_examples(o):
+    """Hand-worked single-group columns."""
+    g = _golden("hand_examples.json")
+    for col in g["columns"]:
+        x = np.array(col["x"], np.float32)
+        xb = synth.to_bf16_bits(x)
+        assert np.array_equal(ref_loop.bf16_bits_to_f32(xb), x)  # bf16-exact
+        q, s = o.colwise(xb.reshape(-1, 1), np.array([x.size], np.int32))
+        want = [int(c, 16) for c in col["q"]]
+        assert q.reshape(-1).tolist() == want, (col["x"], q.reshape(-1), want)
+        if "scale" in col:
+            assert s[0, 0] == np.float32(col["scale"]), (s[0, 0], col["scale"])
+        else:
+            assert hex(int(s[0, 0:1].view(np.uint32)[0])) == col["scale_bits"]
+
+
+# ------------------------------------------------------ whole-path pins --
+
+SMALL_CASES = [
+    # (kind, rows, cols, n_groups, seed, n_empty, align, scale_mix, uncovered)
+    ("colwise", 64, 48, 3, 1, 0, 16, False, 0),
+    ("colwise", 96, 32, 5, 2, 2, 16, True, 0),
+    ("colwise", 80, 16, 4, 3, 1, 16, True, 16),
+    ("colwise", 37, 24, 4, 4, 1, 1, True, 5),
+    ("colwise", 1, 16, 1, 5, 0, 1, False, 0),
+    ("rowwise_t", 48, 64, 3, 6, 0, 16, False, 0),
+    ("rowwise_t", 32, 96, 5, 7, 2, 16, True, 0),
+    ("rowwise_t", 16, 80, 4, 8, 1, 16, True, 16),
+    ("rowwise_t", 24, 41, 4, 9, 1, 1, True, 3),
+]
+
+
+def _small_cases():
+    for k, r, c, g, s, ne, al, mix, unc in SMALL_CASES:
+        yield synth.random_case(k, r, c, g, seed=s, n_empty=ne, align=al,
+                                scale_mix=mix, uncovered=unc)
+
+
+def pin_paths_vs_library_loop(o):
+    """Both paths equal the torch-loop restatement bit for bit on small cases
+    with empty groups, uncovered tail tokens, subnormals and signed zeros;
+    untouched elements keep a sentinel."""
+    for case in _small_cases():
+        fill = np.full((case.x.shape if case.kind == "colwise"
+                        else case.x.shape[::-1]), 0x5A, np.uint8)
+        if case.kind == "colwise":
+            q, s = o.colwise(case.x, case.offs, out=fill)
+            rq, rs = ref_loop.colwise(case.x, case.offs, fill=0x5A)
+        else:
+            q, s = o.rowwise_t(case.x, case.offs, out=fill)
+            rq, rs = ref_loop.rowwise_t(case.x, case.offs, fill=0x5A)
+        assert np.array_equal(q, rq), case.name
+        assert np.array_equal(s.view(np.uint32), rs.view(np.uint32)), case.name
+
+
+def pin_out_of_contract_offsets(o):
+    """Decreasing and out-of-range offsets are read as the running maximum
+    clamped to the extent (the library's documented reading)."""
+    case = synth.random_case("colwise", 64, 16, 4, seed=21)
+    bad = np.array([32, 16, 80, -5], np.int32)  # -> ends 32, 32, 64, 64
+    q, s = o.colwise(case.x, bad)
+    rq, rs = ref_loop.colwise(case.x, np.array([32, 32, 64, 64], np.int32))
+    assert np.array_equal(q, rq) and np.array_equal(s, rs)
+
+
+def pin_transpose_identity(o):
+    """rowwise_t(A) == colwise(A^T) with the scales transposed -- the
+    transpose method of the #2863 page, as an identity between the paths."""
+    for seed in (31, 32):
+        case = synth.random_case("rowwise_t", 40, 112, 6, seed=seed, n_empty=1,
+                                 scale_mix=True)
+        qt, s_r = o.rowwise_t(case.x, case.offs)
+        q, s_c = o.colwise(np.ascontiguousarray(case.x.T), case.offs)
+        assert np.array_equal(qt, q)
+        assert np.array_equal(s_r, s_c.T)
+
+
+def pin_max_code_invariant(o):
+    """Every group column with amax >= 1e-12 contains a +-448 code; no NaN
+    codes appear; all-zero columns give zero codes and the empty-group scale."""
+    case = synth.colwise_outliers()
+    x = case.x[:, :512].copy()
+    q, s = o.colwise(x, case.offs)
+    xf = ref_loop.bf16_bits_to_f32(x)
+    empty_scale = np.float32(448.0) / np.float32(1e-12)
+    assert not np.any((q & 0x7F) == 0x7F)
+    for (a, b), g in zip(ref_loop.bounds(case.offs, x.shape[0]),
+                         range(case.n_groups)):
+        if b == a:
+            assert np.all(s[g] == empty_scale)
+            continue
+        amax = np.abs(xf[a:b]).max(axis=0)
+        nz = amax >= np.float32(1e-12)
+        hit = np.any((q[a:b] & 0x7F) == 0x7E, axis=0)
+        assert np.array_equal(hit[nz], np.ones(nz.sum(), bool)), g
+        assert np.all(q[a:b][:, amax == 0] & 0x7F == 0)
+        assert np.all(s[g][amax == 0] == empty_scale)
+
+
+def pin_dequant_bound(o):
+    """decode(q) / scale is within half an e4m3 ulp of x: relative 2^-4 in
+    the normal range, absolute 2^-10 / scale below it."""
+    case = synth.random_case("colwise", 256, 64, 4, seed=41, scale_mix=True)
+    q, s = o.colwise(case.x, case.offs)
+    xf = ref_loop.bf16_bits_to_f32(case.x).astype(np.float64)
+    for (a, b), g in zip(ref_loop.bounds(case.offs, xf.shape[0]),
+                         range(case.n_groups)):
+        if b == a:
+            continue
+        deq = o.e4m3_decode(q[a:b]) / s[g].astype(np.float64)
+        err = np.abs(deq - xf[a:b])
+        lim = np.maximum(np.abs(xf[a:b]) * 2.0 ** -4,
+                         2.0 ** -10 / s[g].astype(np.float64))
+        assert np.all(err <= lim * (1 + 1e-6)), g
+
+
+ALL_PINS = [
+    pin_decode_landmarks, pin_decode_vs_torch, pin_encode_roundtrip,
+    pin_encode_midpoints, pin_encode_boundaries, pin_encode_vs_torch,
+    pin_scale_exact, pin_quant_single_rounding, pin_hand_examples,
+    pin_paths_vs_library_loop, pin_out_of_contract_offsets,
+    pin_transpose_identity, pin_max_code_invariant, pin_dequant_bound,
+]
