@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of the per-token-group fp8 e4m3 quantization hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  colwise   X (65536, 4096) bf16, 16 token groups along dim0 -> e4m3 + scales
+  rowwise_t A (8192, 16640) bf16, 64 token groups along dim1 (two empty,
+            0.5% outlier columns) -> e4m3 A^T + scales
+the two large workloads of the pytorch/ao PR pages (#2668's (65536, 4096)
+benchmark shape, #2863's (Mg, N) = (16640, 8192) shape).
+
+Metric: achieved HBM GB/s counted algorithmically -- 2 bytes read + 1 byte
+written per element plus 4 bytes per scale (the ideal of one read) -- over
+the device time of the timed steps; also us per call.  Inputs (512 MB and
+272 MB) are larger than L2 (126 MB) and disjoint, so no L2 flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+
+N > 1 runs under torchrun, one rank per GPU, each rank on its own batch
+(weak scaling, no data-path collective); time is the max over ranks.
+``--impl reference`` times the CPU oracle (the plain C statement of the
+method) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("achieved HBM GB/s and % of GB300 peak for per-group fp8 quant "
+          "(algorithmic bytes: 2 B read + 1 B written per element + 4 B per "
+          "scale); us/call")
+UNIT = "GB/s"
+COLWISE_SHAPE = (65536, 4096, 16)   # M, K, groups
+ROWWISE_SHAPE = (8192, 16640, 64)   # N, Mg, groups
+FALLBACK_HBM_GBS = 6800.0
+# pytorch/ao PR pages, hardware unstated: context only
+PAGES_CONTEXT = {
+    "colwise_65536x4096_g16_triton_us": 1603.23,
+    "rowwise_16640x8192_g64_triton_transpose_us": 784.288,
+    "source": "pytorch/ao #2668 new-autotune table; #2863 Benchmarks table",
+}
+KERNEL_SOURCES = ["gq_device.cuh", "gq_colwise.cu", "gq_rowwise.cu"]
+
+
+# ------------------------------------------------------------- helpers --
+
+def colwise_bytes(M, K, G):
+    return 3 * M * K + 4 * G * K
+
+
+def rowwise_bytes(N, Mg, G):
+    return 3 * N * Mg + 4 * N * G
+
+
+def step_bytes():
+    return colwise_bytes(*COLWISE_SHAPE) + rowwise_bytes(*ROWWISE_SHAPE)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "fp8_quantization_moe_gb300", "csrc")
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = d.get(kernel)
+    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec
+
+
+def reduce_over_ranks(ms: float, nbytes: int, dist_ok: bool):
+    """Max of the per-rank timed milliseconds and sum of the per-rank bytes."""
+    if not dist_ok:
+        return ms, nbytes
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    b = torch.tensor([nbytes], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(b.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples in a background process."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+             "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []  # (time, sm, max, reasons)
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.t_load = [None, None]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-i",
+                 self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            reasons = [n for n, v in zip(self.NAMES, parts[4:8]) if v == "Active"]
+            self.samples.append((time.time(), sm, mx, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        t0, t1 = self.t_load
+        load = [s for s in self.samples
+                if t0 is not None and t1 is not None and t0 <= s[0] <= t1]
+        if not load:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0, "note": "no nvidia-smi samples"}
+        reasons = sorted({r for s in load for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in load),
+                "sm_max_mhz": max(s[2] for s in load), "reasons": reasons,
+                "samples": len(load),
+                "window": "sustained run of the same step around the timed "
+                          "region"}
+
+
+# -------------------------------------------------------- the CPU oracle --
+
+def oracle_sample_gbs(budget_s: float = 12.0):
+    """The oracle, as it stands, on bounded samples of the workload: the
+    colwise path on a 512-column slice of X (all 65536 rows, the same 16
+    groups) and the rowwise_t path on a 512-row slice of A (all 16640
+    columns, the same 64 groups).  Returns (GB/s, seconds, sample text)."""
+    import numpy as np
+
+    import oracle
+    from fp8_quantization_moe_gb300 import synth
+
+    M, K, G = COLWISE_SHAPE
+    N, Mg, Gr = ROWWISE_SHAPE
+    kc, nr = 512, 512
+    c = synth.colwise_large(G, rows=M, cols=kc)
+    r = synth.rowwise_outliers(Gr, N=nr, Mg=Mg)
+    o = oracle.get()
+    nbytes, secs = 0, 0.0
+    reps = 0
+    while secs < budget_s or reps == 0:
+        t = time.perf_counter()
+        o.colwise(c.x, c.offs)
+        o.rowwise_t(r.x, r.offs)
+        secs += time.perf_counter() - t
+        nbytes += colwise_bytes(M, kc, G) + rowwise_bytes(nr, Mg, Gr)
+        reps += 1
+        if secs > budget_s / 2 and reps >= 1:
+            break
+    sample = (f"colwise {M}x{kc} (16 groups) + rowwise_t {nr}x{Mg} (64 groups), "
+              f"{reps} pass(es), {secs:.1f} s single-threaded")
+    return nbytes / secs / 1e9, secs, sample
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+
+    import oracle
+    from fp8_quantization_moe_gb300 import synth
+
+    oracle.build()
+    o = oracle.get()
+    M, K, G = COLWISE_SHAPE
+    N, Mg, Gr = ROWWISE_SHAPE
+    kc, nr = 128, 128  # per-step sample: ~1 s of oracle work
+    c = synth.colwise_large(G, rows=M, cols=kc)
+    r = synth.rowwise_outliers(Gr, N=nr, Mg=Mg)
+    per_step = colwise_bytes(M, kc, G) + rowwise_bytes(nr, Mg, Gr)
+    for _ in range(args.warmup):
+        o.colwise(c.x, c.offs)
+        o.rowwise_t(r.x, r.offs)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        o.colwise(c.x, c.offs)
+        o.rowwise_t(r.x, r.offs)
+    secs = time.perf_counter() - t
+    gbs = per_step * args.steps / secs / 1e9
+    sample = (f"per step: colwise {M}x{kc} of X (16 groups) + rowwise_t "
+              f"{nr}x{Mg} of A (64 groups), single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3 (fp32 scale math)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "colwise 65536x4096 g16 + rowwise_t 8192x16640 g64 "
+                   "(bounded column/row samples on the CPU)",
+                   "parallelism": "single CPU thread"},
+        "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": oracle.threads_used(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- GPU path --
+
+def run_mine(args):
+    import numpy as np
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_ok = world > 1
+    if dist_ok:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import fp8_quantization_moe_gb300 as gq
+    from fp8_quantization_moe_gb300 import synth
+
+    M, K, G = COLWISE_SHAPE
+    N, Mg, Gr = ROWWISE_SHAPE
+    seed_off = 7919 * rank  # each rank its own batch
+    c = synth.colwise_large(G, seed=1300 + G + seed_off)
+    r = synth.rowwise_outliers(Gr, seed=1500 + Gr + seed_off)
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x, a = to_dev(c.x), to_dev(r.x)
+    xo = torch.from_numpy(c.offs).to(dev)
+    ao = torch.from_numpy(r.offs).to(dev)
+    q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    qs = torch.empty((G, K), dtype=torch.float32, device=dev)
+    qt = torch.empty((Mg, N), dtype=torch.float8_e4m3fn, device=dev)
+    ts = torch.empty((N, Gr), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gq.colwise(x, xo, out=q, scales=qs, stream=stream)
+        gq.rowwise_t(a, ao, out=qt, scales=ts, stream=stream)
+
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(f"GPU-{props.uuid}")
+    sampler.start()
+    time.sleep(0.3)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    gq.check_device_error()
+
+    # sustained load around the timed region, for the clock samples
+    sampler.t_load[0] = time.time()
+    t_end = time.time() + args.clock_window
+    while time.time() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize(dev)
+
+    if dist_ok:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+          for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        gq.colwise(x, xo, out=q, scales=qs, stream=stream)
+        ev[i][1].record(stream)
+        gq.rowwise_t(a, ao, out=qt, scales=ts, stream=stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist_ok:
+        torch.distributed.barrier()
+    sampler.t_load[1] = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    gq.check_device_error()
+
+    col_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    row_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    nbytes = step_bytes() * args.steps
+    max_ms, all_bytes = reduce_over_ranks(total_ms, nbytes, dist_ok)
+    value = all_bytes / (max_ms * 1e-3) / 1e9
+
+    # end to end through the host-buffer API: H2D inputs, kernels, D2H outputs
+    xh = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ah = torch.from_numpy(r.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    xoh = torch.from_numpy(c.offs).pin_memory()
+    aoh = torch.from_numpy(r.offs).pin_memory()
+    qh = torch.empty((M, K), dtype=torch.float8_e4m3fn, pin_memory=True)
+    qsh = torch.empty((G, K), dtype=torch.float32, pin_memory=True)
+    qth = torch.empty((Mg, N), dtype=torch.float8_e4m3fn, pin_memory=True)
+    tsh = torch.empty((N, Gr), dtype=torch.float32, pin_memory=True)
+
+    def e2e_step():
+        gq.colwise_host(xh, xoh, qh, qsh, device=dev, stream=stream)
+        gq.rowwise_t_host(ah, aoh, qth, tsh, device=dev, stream=stream)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_max, e2e_bytes = reduce_over_ranks(e2e_ms, step_bytes() * args.e2e_steps,
+                                           dist_ok)
+    h2d = (c.x.nbytes + r.x.nbytes + c.offs.nbytes + r.offs.nbytes)
+    d2h = (M * K + G * K * 4 + Mg * N + N * Gr * 4)
+
+    peak, peak_kind = measured_peaks()
+    col_b = colwise_bytes(M, K, G)
+    row_b = rowwise_bytes(N, Mg, Gr)
+    col_avg = statistics.mean(col_ms)
+    row_avg = statistics.mean(row_ms)
+    col_gbs = col_b / (col_avg * 1e-3) / 1e9
+    row_gbs = row_b / (row_avg * 1e-3) / 1e9
+    tr = traffic_record("colwise")
+    tr_row = traffic_record("rowwise_t")
+
+    if rank != 0:
+        if dist_ok:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, secs, sample = oracle_sample_gbs()
+        import oracle
+        cpu = {"value": gbs, "unit": UNIT, "cores": oracle.threads_used(),
+               "kind": "oracle", "sample": sample}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16->e4m3 (fp32 scale math)", "data": "synthetic (seeded)",
+        "config": {
+            "workload": "colwise X 65536x4096 bf16, 16 groups (rows scaled "
+                        "10^U(-2,2)) + rowwise_t A 8192x16640 bf16, 64 groups "
+                        "(2 empty, 0.5% outlier columns x1000)",
+            "global_batch": 65536 + 16640, "parallelism": f"replicas x{world}",
+            "l2": "inputs (512 MB, 272 MB) larger than L2 and disjoint; no flush",
+        },
+        "per_call": {
+            "colwise_us": col_avg * 1e3, "colwise_gbs": col_gbs,
+            "colwise_pct_peak": 100 * col_gbs / peak,
+            "rowwise_t_us": row_avg * 1e3, "rowwise_t_gbs": row_gbs,
+            "rowwise_t_pct_peak": 100 * row_gbs / peak,
+            "timing": "CUDA events on the launching stream around each C-ABI "
+                      "call (workspace clear + kernel)",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "colwise", "achieved": col_gbs,
+            "peak": peak, "unit": "GB/s", "frac": col_gbs / peak,
+            "peak_kind": f"{peak_kind} copy bandwidth (hbm_gbs)",
+            "traffic": (tr["dram_bytes_per_launch"] if tr else None),
+            "algorithmic_bytes": col_b,
+        },
+        "roofline_rowwise_t": {
+            "bound": "hbm", "kernel": "rowwise_t", "achieved": row_gbs,
+            "peak": peak, "unit": "GB/s", "frac": row_gbs / peak,
+            "traffic": (tr_row["dram_bytes_per_launch"] if tr_row else None),
+            "algorithmic_bytes": row_b,
+        },
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_bytes / (e2e_max * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps,
+                "path": "colwise_host + rowwise_t_host (pinned host buffers)"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(),
+        "pages_context": PAGES_CONTEXT,
+        "gpu": props.name,
+    }
+    print(json.dumps(line), flush=True)
+    if dist_ok:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--clock-window", type=float, default=1.5,
+                    help="seconds of sustained load around the timed region")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3  # timing rule: at least three warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_mine(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

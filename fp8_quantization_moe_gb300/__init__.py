@@ -1,1 +1,27 @@
-"""GB300-native per-token-group fp8 e4m3 quantization (placeholder)."""
+"""GB300-native per-token-group fp8 e4m3 quantization for MoE grouped GEMMs.
+
+Two paths, both in hand-written sm_103a CUDA kernels behind the C ABI of
+``include/gq_fp8.h``:
+
+* ``colwise(x, offs)``   -- groups along dim0: one scale per (group, column);
+* ``rowwise_t(a, offs)`` -- groups along dim1: one scale per (row, group), fp8
+  output written transposed.
+
+scale = 448 / max(amax, 1e-12) in IEEE fp32; q = saturating round-to-nearest-
+even e4m3 cast of fp32(x * scale).  ``offs`` are int32 end offsets of the
+token groups.  This package is argument marshalling over the library; torch
+supplies device memory and streams.  ``synth`` draws seeded inputs.
+"""
+from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
+                       GQError, check_device_error, colwise, colwise_host,
+                       debug_set, lib, library_path, rowwise_t,
+                       rowwise_t_host, status_string, version,
+                       workspace_bytes)
+from ._build import build
+
+__all__ = [
+    "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQError",
+    "build", "check_device_error", "colwise", "colwise_host", "debug_set",
+    "lib", "library_path", "rowwise_t", "rowwise_t_host", "status_string",
+    "version", "workspace_bytes",
+]

@@ -1,0 +1,276 @@
+"""ctypes binding over the C ABI of libgqfp8 (include/gq_fp8.h).
+
+Argument marshalling only: every step of the quantization runs in the
+library's CUDA kernels.  torch supplies device memory and streams.  There is
+no CPU fallback: without the compiled library or a CUDA device the calls
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+GQ_OK = 0
+GQ_ERR_INVALID_ARG = 1
+GQ_ERR_UNSUPPORTED = 2
+GQ_ERR_CUDA = 3
+GQ_ERR_TIMEOUT = 4
+GQ_KIND_COLWISE = 0
+GQ_KIND_ROWWISE_T = 1
+GQ_MAX_GROUPS = 1024
+
+# Every symbol the header declares, with its ctypes signature.
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+SIGNATURES = {
+    "gq_workspace_bytes": (_SZ, [ctypes.c_int, _I64, _I64, _I32]),
+    "gq_fp8_colwise": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "gq_fp8_rowwise_t": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "gq_check_device_error": (ctypes.c_int, [_P]),
+    "gq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gq_last_error": (ctypes.c_char_p, []),
+    "gq_version": (ctypes.c_int, []),
+    "gq_debug_set": (ctypes.c_int, [ctypes.c_int, _I64]),
+}
+
+
+class GQError(RuntimeError):
+    """A non-OK status from libgqfp8."""
+
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({detail})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libgqfp8 is not built ({path} missing); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            handle = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != GQ_OK:
+        L = lib()
+        detail = (L.gq_status_string(status) or b"").decode()
+        msg = (L.gq_last_error() or b"").decode()
+        raise GQError(status, where, f"{detail}: {msg}" if msg else detail)
+
+
+def status_string(status: int) -> str:
+    return lib().gq_status_string(status).decode()
+
+
+def version() -> int:
+    return lib().gq_version()
+
+
+def workspace_bytes(kind: int, rows: int, cols: int, n_groups: int) -> int:
+    return int(lib().gq_workspace_bytes(kind, rows, cols, n_groups))
+
+
+# ----------------------------------------------------------- workspaces --
+_ws_cache: dict = {}
+_ws_lock = threading.Lock()
+
+
+def _workspace(nbytes: int, device: torch.device, stream_handle: int):
+    """A cached device workspace per (device, stream); the library clears it
+    on every call, so reuse across calls on one stream is safe."""
+    if nbytes == 0:
+        return None
+    key = (device.index, stream_handle)
+    with _ws_lock:
+        buf = _ws_cache.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+            _ws_cache[key] = buf
+    return buf
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream, device):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return s.cuda_stream
+
+
+def _ws_ptr(buf):
+    if buf is None:
+        return None, 0
+    p = buf.data_ptr()
+    aligned = (p + 255) & ~255
+    return aligned, buf.numel() - (aligned - p)
+
+
+def _check_in(x, offs, name):
+    if not (isinstance(x, torch.Tensor) and x.is_cuda):
+        raise ValueError(f"{name}: input must be a CUDA tensor")
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError(f"{name}: input must be a contiguous 2-D bf16 tensor")
+    if not (isinstance(offs, torch.Tensor) and offs.is_cuda
+            and offs.dtype == torch.int32 and offs.dim() == 1
+            and offs.is_contiguous() and offs.device == x.device):
+        raise ValueError(f"{name}: offs must be a contiguous 1-D int32 tensor "
+                         "on the input's device")
+
+
+# ---------------------------------------------------------------- paths --
+
+def colwise(x: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
+            stream=None, workspace=None):
+    """Colwise per-token-group scaling (groups along dim0).
+
+    x: bf16 (M, K) CUDA tensor; offs: int32 (n_groups,) end offsets on the
+    same device.  Returns (q float8_e4m3fn (M, K), scales float32
+    (n_groups, K)).  Rows outside every group keep the contents of ``out``
+    (uninitialised when ``out`` is None).  Asynchronous on ``stream`` (default:
+    the current stream).
+    """
+    _check_in(x, offs, "colwise")
+    M, K = x.shape
+    G = offs.numel()
+    dev = x.device
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    if scales is None:
+        scales = torch.empty((G, K), dtype=torch.float32, device=dev)
+    if out.shape != (M, K) or out.element_size() != 1 or not out.is_contiguous():
+        raise ValueError("colwise: out must be a contiguous 1-byte (M, K) tensor")
+    if scales.shape != (G, K) or scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError("colwise: scales must be a contiguous float32 (G, K) tensor")
+    sh = _stream_handle(stream, dev)
+    need = workspace_bytes(GQ_KIND_COLWISE, M, K, G)
+    ws = workspace if workspace is not None else _workspace(need, dev, sh)
+    wp, wn = _ws_ptr(ws)
+    with torch.cuda.device(dev):
+        st = lib().gq_fp8_colwise(_ptr(x), M, K, _ptr(offs), G, _ptr(out),
+                                  _ptr(scales), wp, wn, sh)
+    _check(st, "gq_fp8_colwise")
+    return out, scales
+
+
+def rowwise_t(a: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
+              stream=None, workspace=None):
+    """Rowwise per-token-group scaling with transposed output (groups along
+    dim1 of A).
+
+    a: bf16 (N, Mg) CUDA tensor; offs: int32 (n_groups,) end offsets along
+    Mg.  Returns (qt float8_e4m3fn (Mg, N) = q(a)^T, scales float32
+    (N, n_groups)).  Token rows of qt outside every group keep ``out``.
+    """
+    _check_in(a, offs, "rowwise_t")
+    N, Mg = a.shape
+    G = offs.numel()
+    dev = a.device
+    if out is None:
+        out = torch.empty((Mg, N), dtype=torch.float8_e4m3fn, device=dev)
+    if scales is None:
+        scales = torch.empty((N, G), dtype=torch.float32, device=dev)
+    if out.shape != (Mg, N) or out.element_size() != 1 or not out.is_contiguous():
+        raise ValueError("rowwise_t: out must be a contiguous 1-byte (Mg, N) tensor")
+    if scales.shape != (N, G) or scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError("rowwise_t: scales must be a contiguous float32 (N, G) tensor")
+    sh = _stream_handle(stream, dev)
+    need = workspace_bytes(GQ_KIND_ROWWISE_T, N, Mg, G)
+    ws = workspace if workspace is not None else _workspace(need, dev, sh)
+    wp, wn = _ws_ptr(ws)
+    with torch.cuda.device(dev):
+        st = lib().gq_fp8_rowwise_t(_ptr(a), N, Mg, _ptr(offs), G, _ptr(out),
+                                    _ptr(scales), wp, wn, sh)
+    _check(st, "gq_fp8_rowwise_t")
+    return out, scales
+
+
+def check_device_error(stream=None, device=None):
+    """Synchronises the stream and raises GQError on a recorded device-side
+    timeout (or a CUDA error)."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    sh = _stream_handle(stream, dev)
+    with torch.cuda.device(dev):
+        _check(lib().gq_check_device_error(sh), "gq_check_device_error")
+
+
+def debug_set(skip_arrival: bool = False, wait_timeout_ns: int = 0):
+    """Test hook: see gq_debug_set in include/gq_fp8.h."""
+    _check(lib().gq_debug_set(int(bool(skip_arrival)), int(wait_timeout_ns)),
+           "gq_debug_set")
+
+
+# ------------------------------------------------------ host-buffer calls --
+
+def _to_device(t, device, name):
+    if t.is_cuda:
+        raise ValueError(f"{name}: expected a host tensor")
+    return t.to(device, non_blocking=True)
+
+
+def colwise_host(x_host, offs_host, out_host=None, scales_host=None, *,
+                 device="cuda", stream=None):
+    """End-to-end colwise call on host buffers: host->device copies of x and
+    offs, the kernel, device->host copies of q and scales, all enqueued on
+    ``stream``.  Pinned host tensors make the copies asynchronous; the caller
+    synchronises before reading the results."""
+    dev = torch.device(device)
+    M, K = x_host.shape
+    G = offs_host.numel()
+    if out_host is None:
+        out_host = torch.empty((M, K), dtype=torch.float8_e4m3fn, pin_memory=True)
+    if scales_host is None:
+        scales_host = torch.empty((G, K), dtype=torch.float32, pin_memory=True)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    with torch.cuda.stream(s):
+        x = _to_device(x_host, dev, "colwise_host")
+        o = _to_device(offs_host, dev, "colwise_host")
+        q, sc = colwise(x, o, stream=s)
+        out_host.copy_(q, non_blocking=True)
+        scales_host.copy_(sc, non_blocking=True)
+    return out_host, scales_host
+
+
+def rowwise_t_host(a_host, offs_host, out_host=None, scales_host=None, *,
+                   device="cuda", stream=None):
+    """End-to-end rowwise_t call on host buffers (see colwise_host)."""
+    dev = torch.device(device)
+    N, Mg = a_host.shape
+    G = offs_host.numel()
+    if out_host is None:
+        out_host = torch.empty((Mg, N), dtype=torch.float8_e4m3fn, pin_memory=True)
+    if scales_host is None:
+        scales_host = torch.empty((N, G), dtype=torch.float32, pin_memory=True)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    with torch.cuda.stream(s):
+        a = _to_device(a_host, dev, "rowwise_t_host")
+        o = _to_device(offs_host, dev, "rowwise_t_host")
+        qt, sc = rowwise_t(a, o, stream=s)
+        out_host.copy_(qt, non_blocking=True)
+        scales_host.copy_(sc, non_blocking=True)
+    return out_host, scales_host

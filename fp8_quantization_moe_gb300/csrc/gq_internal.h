@@ -1,0 +1,74 @@
+// gq_internal.h -- host-side declarations shared by the translation units of
+// libgqfp8 (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gq_fp8.h"
+
+namespace gq {
+
+// Per-device facts and handles, filled once per device.
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  unsigned* err_word = nullptr;  // device address of the error word
+  int colwise_ctas_per_sm = 0;
+  int rowwise_ctas_per_sm = 0;
+};
+
+// Launch-time knobs (test hooks).
+struct DebugKnobs {
+  int skip_arrival = 0;
+  uint64_t timeout_ns = 1000000000ull;
+};
+
+// Encodes a 2-D tiled tensor map (row-major, dim0 innermost).
+gq_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype,
+                          void* base, uint64_t dim0, uint64_t dim1,
+                          uint64_t row_stride_bytes, uint32_t box0,
+                          uint32_t box1, CUtensorMapSwizzle swizzle);
+
+// Records a message for gq_last_error() and returns `st`.
+gq_status fail(gq_status st, const char* fmt, ...);
+
+// Returns GQ_ERR_CUDA with the runtime's message if `e` is an error.
+gq_status check_cuda(cudaError_t e, const char* what);
+
+// Workspace layout shared by both paths: a 256-byte counter header (ticket
+// counter first), then one done-counter per dependency group, then the amax
+// words.  Offsets in bytes.
+struct WorkspaceLayout {
+  size_t counters = 0;  // start of the done counters
+  size_t amax = 0;      // start of the amax words
+  size_t total = 0;
+};
+WorkspaceLayout workspace_layout(int64_t dep_groups, int64_t amax_words);
+
+namespace colwise {
+constexpr int kW = 128;  // columns per slab
+constexpr int kR = 64;   // token rows per tile
+gq_status setup(DeviceInfo& info);
+gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
+                 int32_t M, int32_t K, const int32_t* offs, int32_t G,
+                 void* out, float* scales, void* ws, cudaStream_t stream);
+}  // namespace colwise
+
+namespace rowwise {
+constexpr int kTn = 128;  // rows of A per tile (bytes per output row run)
+constexpr int kTm = 64;   // token columns per tile
+gq_status setup(DeviceInfo& info);
+gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
+                 int32_t N, int32_t Mg, const int32_t* offs, int32_t G,
+                 void* out_t, float* scales, void* ws, cudaStream_t stream);
+}  // namespace rowwise
+
+// Writes 448 / 1e-12 (fp32) into n scales: every group is empty when the
+// token extent is 0.
+gq_status launch_fill_empty_scales(float* scales, int64_t n,
+                                   cudaStream_t stream);
+
+}  // namespace gq

@@ -1,0 +1,166 @@
+/*
+ * gq_fp8.h -- C ABI of libgqfp8: per-token-group fp8 e4m3 quantization for
+ * the grouped GEMMs of MoE fp8 training, on GB300 (sm_103a).
+ *
+ * The method comes from two pytorch/ao pull-request pages:
+ *   [moe training] "use smaller block sizes for per group scaling kernels to
+ *       improve perf" (#2668): intro (the per-token-group scaling kernel along
+ *       dim0, and its "grid too small" finding) and the kernel arguments in
+ *       its torch.compile failure report (fp8_dtype_max = 448.0,
+ *       fp8_dtype_min = -448.0, EPS = 1e-12);
+ *   [moe fp8 training] "test and bench new faster method for per group
+ *       rowwise scaling" (#2863): Summary (per-group rowwise scaling for the
+ *       backward grad_weight = grad_output_t @ input GEMM, computed through
+ *       the transpose so that global accesses stay coalesced).
+ *
+ * For a token group g = [s_g, e_g) and each column (colwise) or row
+ * (rowwise):
+ *     amax  = max |x| over the group's tokens (0 when the group is empty)
+ *     scale = 448 / max(amax, 1e-12)                      IEEE fp32 division
+ *     q     = e4m3(fp32(x * scale))                       fp32 multiply, then
+ *             round-to-nearest-even, saturating to +-448
+ * The stored scale is that multiplier; dequantization divides by it.
+ *
+ * Token groups.  `offs` holds n_groups int32 END offsets on the device:
+ * group 0 is [0, offs[0]), group g is [offs[g-1], offs[g]).  Contract:
+ * nondecreasing, offs[n_groups-1] <= extent (M for colwise, Mg for
+ * rowwise_t).  The library never reads offs on the host (that would need a
+ * device synchronisation); the kernels read each end as the running maximum
+ * of offs[0..g] clamped to [0, extent], so out-of-contract offsets cannot
+ * cause an out-of-bounds access.  Tokens past the last end belong to no
+ * group: their output bytes are left untouched.  Groups need not be
+ * multiples of 16 tokens (the MoE training test aligns them to 16; these
+ * kernels do not rely on it).
+ *
+ * Memory.  Every pointer is device memory that the caller allocates and
+ * owns; the library allocates nothing and does not synchronise the host on
+ * the quantization calls, which are asynchronous on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream).  Outputs and the
+ * workspace must stay valid until the stream's work completes.  Concurrent
+ * calls must use distinct workspaces.
+ *
+ * Errors.  Every condition the host can check returns a status before any
+ * work is enqueued; nothing aborts.  Failures of the CUDA runtime during
+ * set-up or launch return GQ_ERR_CUDA, with detail in gq_last_error().  A
+ * kernel that waits on another thread block gives up after a bounded time
+ * (default 1 s): it then records GQ_ERR_TIMEOUT in a per-device error word,
+ * finishes without hanging, and gq_check_device_error() reports it.
+ */
+#ifndef GQ_FP8_H
+#define GQ_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* gq_stream_t;
+
+typedef enum gq_status {
+  GQ_OK = 0,
+  GQ_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment,
+                             workspace too small */
+  GQ_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle:
+                             n_groups > GQ_MAX_GROUPS, K % 16, N % 16,
+                             Mg % 8, an extent >= 2^31, no sm_103 device */
+  GQ_ERR_CUDA = 3,        /* CUDA runtime failure (see gq_last_error) */
+  GQ_ERR_TIMEOUT = 4      /* a bounded cross-block wait expired on the GPU */
+} gq_status;
+
+#define GQ_KIND_COLWISE 0
+#define GQ_KIND_ROWWISE_T 1
+#define GQ_MAX_GROUPS 1024
+
+/*
+ * Workspace size in bytes for one call.
+ *   kind GQ_KIND_COLWISE:   rows = M, cols = K.
+ *   kind GQ_KIND_ROWWISE_T: rows = N, cols = Mg.
+ * The workspace holds the per-(group, column) or per-(row, group) running
+ * amax words and the work-claiming counters; the call clears it itself, so
+ * its contents on entry do not matter.  Returns 0 when no workspace is
+ * needed (empty problems) and for invalid arguments.
+ */
+size_t gq_workspace_bytes(int kind, int64_t rows, int64_t cols,
+                          int32_t n_groups);
+
+/*
+ * Colwise per-token-group scaling: groups run along dim0 (the token rows),
+ * one scale per (group, column).  The dim0 kernel of pytorch/ao #2668.
+ *
+ *   x        bf16 [M, K] row-major, 16-byte aligned base.       (input)
+ *   M, K     M >= 0 tokens; K >= 0 columns, K % 16 == 0.
+ *   offs     int32 [n_groups] end offsets along M, device.      (input)
+ *   n_groups 1 <= n_groups <= GQ_MAX_GROUPS.
+ *   out      e4m3 bytes [M, K] row-major, 16-byte aligned.       (output)
+ *            out[r][k] = q(x[r][k]) for every r inside a group.
+ *   scales   fp32 [n_groups, K] row-major, 4-byte aligned.       (output)
+ *            Every entry is written, empty groups included
+ *            (448 / 1e-12 rounded to fp32).
+ *   workspace, workspace_bytes: at least gq_workspace_bytes(GQ_KIND_COLWISE,
+ *            M, K, n_groups) bytes, 256-byte aligned (may be NULL when that
+ *            is 0).
+ *   stream   the CUDA stream to run on.
+ */
+gq_status gq_fp8_colwise(const void* x, int64_t M, int64_t K,
+                         const int32_t* offs, int32_t n_groups, void* out,
+                         float* scales, void* workspace,
+                         size_t workspace_bytes, gq_stream_t stream);
+
+/*
+ * Rowwise per-token-group scaling with transposed output: groups run along
+ * dim1 (the Mg token columns of A), one scale per (row, group), and the fp8
+ * result is written as A^T -- the operand layout the backward grad_weight
+ * GEMM of pytorch/ao #2863 consumes.
+ *
+ *   a        bf16 [N, Mg] row-major, 16-byte aligned base.      (input)
+ *   N, Mg    N >= 0 rows, N % 16 == 0; Mg >= 0 tokens, Mg % 8 == 0.
+ *   offs     int32 [n_groups] end offsets along Mg, device.     (input)
+ *   n_groups 1 <= n_groups <= GQ_MAX_GROUPS.
+ *   out_t    e4m3 bytes [Mg, N] row-major, 16-byte aligned.      (output)
+ *            out_t[m][n] = q(a[n][m]) for every token m inside a group.
+ *   scales   fp32 [N, n_groups] row-major, 4-byte aligned.       (output)
+ *            Every entry is written, empty groups included.
+ *   workspace, workspace_bytes: at least gq_workspace_bytes(
+ *            GQ_KIND_ROWWISE_T, N, Mg, n_groups) bytes, 256-byte aligned.
+ *   stream   the CUDA stream to run on.
+ */
+gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,
+                           const int32_t* offs, int32_t n_groups, void* out_t,
+                           float* scales, void* workspace,
+                           size_t workspace_bytes, gq_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns GQ_ERR_TIMEOUT if any kernel since the last check gave up a
+ * bounded wait, GQ_ERR_CUDA if the stream reports an error, else GQ_OK.
+ * Not for the hot path: it blocks the host.
+ */
+gq_status gq_check_device_error(gq_stream_t stream);
+
+/* Static English text for a status code. */
+const char* gq_status_string(gq_status status);
+
+/* Detail for the calling thread's last non-OK status ("" if none). */
+const char* gq_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gq_version(void);
+
+/*
+ * Test hook for the bounded cross-block waits.  wait_timeout_ns sets the
+ * limit after which a waiting kernel gives up (0 restores the 1 s default).
+ * skip_arrival != 0 makes the next launches omit one thread block's
+ * completion signal -- the first phase-A tile of the first column slab (or
+ * row band) -- so that its waiters must time out and report
+ * GQ_ERR_TIMEOUT.  Process-wide; not thread-safe with concurrent calls.
+ */
+gq_status gq_debug_set(int skip_arrival, int64_t wait_timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQ_FP8_H */

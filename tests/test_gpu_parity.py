@@ -1,0 +1,278 @@
+"""GPU path against the oracle, through the C ABI (needs an sm_103 GPU).
+
+Bit-exact comparison of every fp8 byte and every fp32 scale bit pattern: the
+method is deterministic (max is order-independent, the scale is one IEEE
+division, the product one IEEE multiply, the cast one RNE step), so the bar is
+exact equality, and untouched output bytes must keep a sentinel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_quantization_moe_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 0x5A
+
+
+@pytest.fixture(scope="module")
+def gq():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import fp8_quantization_moe_gb300 as m
+
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    return m
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+        torch.bfloat16).cuda()
+
+
+def dev_i32(a) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+
+
+def run_colwise(gq, x_bits, offs, fill=SENTINEL):
+    M, K = x_bits.shape
+    out = torch.full((M, K), fill, dtype=torch.uint8, device="cuda")
+    q, s = gq.colwise(dev_bf16(x_bits), dev_i32(offs),
+                      out=out.view(torch.float8_e4m3fn))
+    gq.check_device_error()
+    return q.view(torch.uint8).cpu().numpy(), s.cpu().numpy()
+
+
+def run_rowwise(gq, a_bits, offs, fill=SENTINEL):
+    N, Mg = a_bits.shape
+    out = torch.full((Mg, N), fill, dtype=torch.uint8, device="cuda")
+    q, s = gq.rowwise_t(dev_bf16(a_bits), dev_i32(offs),
+                        out=out.view(torch.float8_e4m3fn))
+    gq.check_device_error()
+    return q.view(torch.uint8).cpu().numpy(), s.cpu().numpy()
+
+
+def assert_same(q, s, rq, rs, what):
+    if not np.array_equal(q, rq):
+        bad = np.argwhere(q != rq)
+        i = tuple(bad[0])
+        raise AssertionError(f"{what}: {len(bad)} fp8 bytes differ; first at "
+                             f"{i}: gpu {q[i]:#x} oracle {rq[i]:#x}")
+    su, ru = s.view(np.uint32), rs.view(np.uint32)
+    if not np.array_equal(su, ru):
+        bad = np.argwhere(su != ru)
+        i = tuple(bad[0])
+        raise AssertionError(f"{what}: {len(bad)} scales differ; first at {i}: "
+                             f"gpu {s[i]!r} oracle {rs[i]!r}")
+
+
+def check_colwise(gq, case):
+    q, s = run_colwise(gq, case.x, case.offs)
+    fill = np.full(case.x.shape, SENTINEL, np.uint8)
+    rq, rs = oracle.colwise(case.x, case.offs, out=fill)
+    assert_same(q, s, rq, rs, case.name)
+
+
+def check_rowwise(gq, case):
+    q, s = run_rowwise(gq, case.x, case.offs)
+    fill = np.full(case.x.shape[::-1], SENTINEL, np.uint8)
+    rq, rs = oracle.rowwise_t(case.x, case.offs, out=fill)
+    assert_same(q, s, rq, rs, case.name)
+
+
+# --------------------------------------------------------- small / ragged --
+# Sizes span several 64x128 (colwise) or 128x64 (rowwise) tiles with ragged
+# tails; groups include empty ones, unaligned boundaries and uncovered tails.
+COLWISE_CASES = [
+    # rows, cols, groups, seed, n_empty, align, scale_mix, uncovered
+    (200, 272, 4, 1, 1, 16, True, 0),
+    (1000, 384, 7, 2, 2, 1, True, 0),
+    (513, 144, 3, 3, 0, 1, False, 29),
+    (64, 128, 1, 4, 0, 16, False, 0),
+    (1, 16, 1, 5, 0, 1, False, 0),
+    (3, 16, 2, 6, 0, 1, True, 0),
+    (130, 32, 40, 7, 5, 1, True, 0),      # many tiny groups, many per tile
+    (4096, 256, 16, 8, 1, 16, True, 0),
+    (777, 2064, 9, 9, 2, 1, True, 13),
+]
+
+ROWWISE_CASES = [
+    (144, 200, 4, 11, 1, 8, True, 0),
+    (256, 520, 7, 12, 2, 8, True, 0),
+    (16, 8, 1, 13, 0, 8, False, 0),
+    (384, 1000, 5, 14, 0, 8, False, 40),
+    (128, 64, 1, 15, 0, 8, False, 0),
+    (48, 392, 60, 16, 10, 1, True, 0),    # > 8 segments in a tile
+    (2064, 1040, 16, 17, 1, 16, True, 0),
+    (160, 2048, 33, 18, 3, 1, True, 7),
+]
+
+
+@pytest.mark.parametrize("spec", COLWISE_CASES, ids=lambda s: f"{s[0]}x{s[1]}g{s[2]}")
+def test_colwise_small(gq, spec):
+    r, c, g, seed, ne, al, mix, unc = spec
+    check_colwise(gq, synth.random_case("colwise", r, c, g, seed, n_empty=ne,
+                                        align=al, scale_mix=mix, uncovered=unc))
+
+
+@pytest.mark.parametrize("spec", ROWWISE_CASES, ids=lambda s: f"{s[0]}x{s[1]}g{s[2]}")
+def test_rowwise_small(gq, spec):
+    r, c, g, seed, ne, al, mix, unc = spec
+    check_rowwise(gq, synth.random_case("rowwise_t", r, c, g, seed, n_empty=ne,
+                                        align=al, scale_mix=mix, uncovered=unc))
+
+
+# ------------------------------------------------------------ edge cases --
+
+def test_colwise_no_tokens(gq):
+    """M = 0: every group is empty; all scales are 448 / 1e-12."""
+    x = np.zeros((0, 64), np.uint16)
+    q, s = run_colwise(gq, x, np.array([0, 0, 0], np.int32))
+    _, rs = oracle.colwise(x, np.array([0, 0, 0], np.int32))
+    assert q.shape == (0, 64)
+    assert np.array_equal(s.view(np.uint32), rs.view(np.uint32))
+
+
+def test_rowwise_no_tokens(gq):
+    a = np.zeros((32, 0), np.uint16)
+    q, s = run_rowwise(gq, a, np.array([0, 0], np.int32))
+    _, rs = oracle.rowwise_t(a, np.array([0, 0], np.int32))
+    assert q.shape == (0, 32)
+    assert np.array_equal(s.view(np.uint32), rs.view(np.uint32))
+
+
+def test_empty_columns_and_rows(gq):
+    q, s = run_colwise(gq, np.zeros((5, 0), np.uint16), np.array([5], np.int32))
+    assert q.shape == (5, 0) and s.shape == (1, 0)
+    q, s = run_rowwise(gq, np.zeros((0, 24), np.uint16), np.array([24], np.int32))
+    assert q.shape == (24, 0) and s.shape == (0, 1)
+
+
+@pytest.mark.parametrize("offs", [[40, 20, 100, 90], [-5, 64, 64, 300],
+                                  [0, 0, 0, 0], [96, 96, 96, 96]])
+def test_out_of_contract_offsets(gq, offs):
+    """Offsets are read as a running maximum clamped to [0, extent]."""
+    c = synth.random_case("colwise", 96, 48, 1, seed=51)
+    r = synth.random_case("rowwise_t", 32, 96, 1, seed=52)
+    o = np.array(offs, np.int32)
+    check_colwise(gq, synth.Case("oob_c", "colwise", c.x, o, 0))
+    check_rowwise(gq, synth.Case("oob_r", "rowwise_t", r.x, o, 0))
+
+
+def test_single_token_groups(gq):
+    o = np.arange(1, 41, dtype=np.int32)
+    c = synth.random_case("colwise", 40, 32, 1, seed=53, scale_mix=True)
+    check_colwise(gq, synth.Case("tok1_c", "colwise", c.x, o, 0))
+    r = synth.random_case("rowwise_t", 16, 40, 1, seed=54, scale_mix=True)
+    check_rowwise(gq, synth.Case("tok1_r", "rowwise_t", r.x, o, 0))
+
+
+def test_max_groups(gq):
+    """GQ_MAX_GROUPS groups of one or zero tokens."""
+    G = gq.GQ_MAX_GROUPS
+    rng = np.random.default_rng(55)
+    o = np.sort(rng.integers(0, 800, size=G)).astype(np.int32)
+    c = synth.random_case("colwise", 800, 16, 1, seed=56)
+    check_colwise(gq, synth.Case("maxg_c", "colwise", c.x, o, 0))
+    r = synth.random_case("rowwise_t", 16, 800, 1, seed=57)
+    check_rowwise(gq, synth.Case("maxg_r", "rowwise_t", r.x, o, 0))
+
+
+def test_element_map_exhaustive_amax(gq):
+    """Every finite non-negative bf16 value as a column amax, each with 127
+    elements of magnitude at most that amax (both signs, zeros, subnormals,
+    the amax itself): the elementwise map (x, amax) -> q, and every scale,
+    against the oracle -- through both paths."""
+    rng = np.random.default_rng(58)
+    amax = np.arange(0, 0x7F80, dtype=np.uint16)  # 32640 columns
+    K = amax.size
+    R = 128
+    mag = rng.integers(0, 1 << 15, size=(R, K), dtype=np.uint32).astype(np.uint16)
+    mag = np.minimum(mag, amax[None, :])
+    mag[1] = amax            # the amax itself
+    mag[2] = 0               # zero
+    mag[3] = amax // 2       # half the bit pattern: spans binades
+    mag[4] = np.minimum(amax, rng.integers(0, 0x80, size=K).astype(np.uint16))  # subnormals
+    sign = (rng.integers(0, 2, size=(R, K)) << 15).astype(np.uint16)
+    x = mag | sign
+    x[0] = amax              # row 0 carries the amax, positive
+    case = synth.Case("elemmap_c", "colwise", x, np.array([R], np.int32), 0)
+    check_colwise(gq, case)
+    caseT = synth.Case("elemmap_r", "rowwise_t", np.ascontiguousarray(x.T),
+                       np.array([R], np.int32), 0)
+    check_rowwise(gq, caseT)
+
+
+def test_deterministic_and_stream(gq):
+    """Two calls, on a side stream, give identical bytes."""
+    c = synth.random_case("colwise", 2048, 512, 8, seed=59, scale_mix=True)
+    x, o = dev_bf16(c.x), dev_i32(c.offs)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        q1, s1 = gq.colwise(x, o, stream=s)
+        q2, s2 = gq.colwise(x, o, stream=s)
+    s.synchronize()
+    gq.check_device_error(stream=s)
+    assert torch.equal(q1.view(torch.uint8), q2.view(torch.uint8))
+    assert torch.equal(s1, s2)
+
+
+def test_guard_bytes_untouched(gq):
+    """Outputs placed inside a larger buffer: the bytes around them stay."""
+    c = synth.random_case("colwise", 300, 160, 3, seed=60)
+    M, K = c.x.shape
+    buf = torch.full((M * K + 512,), 0xA5, dtype=torch.uint8, device="cuda")
+    out = buf[256:256 + M * K].view(M, K)
+    sbuf = torch.full((3 * K + 128,), -7.0, dtype=torch.float32, device="cuda")
+    sc = sbuf[64:64 + 3 * K].view(3, K)
+    gq.colwise(dev_bf16(c.x), dev_i32(c.offs), out=out.view(torch.float8_e4m3fn),
+               scales=sc)
+    gq.check_device_error()
+    b = buf.cpu().numpy()
+    assert np.all(b[:256] == 0xA5) and np.all(b[256 + M * K:] == 0xA5)
+    sb = sbuf.cpu().numpy()
+    assert np.all(sb[:64] == -7.0) and np.all(sb[64 + 3 * K:] == -7.0)
+    rq, rs = oracle.colwise(c.x, c.offs)
+    assert np.array_equal(b[256:256 + M * K].reshape(M, K), rq)
+
+
+def test_timeout_is_reported_not_hung(gq):
+    """A withheld completion signal makes the waiting blocks give up after
+    the (shortened) limit and report GQ_ERR_TIMEOUT; the next call is fine."""
+    c = synth.random_case("colwise", 1024, 256, 4, seed=61)
+    r = synth.random_case("rowwise_t", 256, 512, 4, seed=62)
+    try:
+        gq.debug_set(skip_arrival=True, wait_timeout_ns=5_000_000)
+        gq.colwise(dev_bf16(c.x), dev_i32(c.offs))
+        with pytest.raises(gq.GQError) as e:
+            gq.check_device_error()
+        assert e.value.status == 4
+        gq.rowwise_t(dev_bf16(r.x), dev_i32(r.offs))
+        with pytest.raises(gq.GQError) as e:
+            gq.check_device_error()
+        assert e.value.status == 4
+    finally:
+        gq.debug_set(False, 0)
+    check_colwise(gq, c)
+    check_rowwise(gq, r)
+
+
+def test_host_buffer_calls(gq):
+    """The end-to-end host-buffer entry points."""
+    c = synth.random_case("colwise", 640, 256, 5, seed=63)
+    xh = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    oh = torch.from_numpy(c.offs).pin_memory()
+    q, s = gq.colwise_host(xh, oh)
+    torch.cuda.synchronize()
+    rq, rs = oracle.colwise(c.x, c.offs)
+    assert_same(q.view(torch.uint8).numpy(), s.numpy(), rq, rs, "colwise_host")
+    r = synth.random_case("rowwise_t", 256, 640, 5, seed=64)
+    ah = torch.from_numpy(r.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    oh = torch.from_numpy(r.offs).pin_memory()
+    q, s = gq.rowwise_t_host(ah, oh)
+    torch.cuda.synchronize()
+    rq, rs = oracle.rowwise_t(r.x, r.offs)
+    assert_same(q.view(torch.uint8).numpy(), s.numpy(), rq, rs, "rowwise_t_host")

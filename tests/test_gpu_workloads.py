@@ -1,0 +1,104 @@
+"""The five workloads at full size, in the launch configuration the benchmark
+times (needs an sm_103 GPU).
+
+The two small workloads are compared with the oracle in full.  The large
+ones are compared on sampled outputs the oracle computes exactly -- whole
+column slabs / row bands at both ends plus random columns / rows (a column of
+colwise, or a row of rowwise_t, depends on nothing else) -- and checked at
+full size against properties that hold at any size: every group column (or
+row) with amax >= 1e-12 holds a +-448 code, no NaN code appears, and
+rowwise_t(A) equals colwise(A^T) with transposed scales.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_quantization_moe_gb300 import synth
+from test_gpu_parity import (SENTINEL, assert_same, check_colwise,
+                             check_rowwise, dev_bf16, dev_i32)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gq():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import fp8_quantization_moe_gb300 as m
+
+    return m
+
+
+def _sample(rng, extent, tile, n_random):
+    idx = set(range(min(tile, extent)))
+    idx |= set(range(max(0, extent - tile), extent))
+    idx |= set(rng.choice(extent, size=min(n_random, extent), replace=False).tolist())
+    return np.array(sorted(idx))
+
+
+def _max_code_property(q_dev: torch.Tensor, x_dev: torch.Tensor, offs, dim):
+    """Per group: columns (dim 0 groups) or rows (dim 1 groups) with
+    amax >= 1e-12 contain a +-448 code (0x7E/0xFE); no NaN codes anywhere."""
+    qm = q_dev.view(torch.uint8) & 0x7F
+    assert not bool((qm == 0x7F).any())
+    prev = 0
+    extent = x_dev.shape[dim]
+    for e in offs.tolist():
+        e = min(max(e, prev), extent)
+        if e > prev:
+            if dim == 0:
+                xs = x_dev[prev:e].float().abs().amax(dim=0)
+                qs = qm[prev:e].amax(dim=0)
+            else:  # x (N, Mg), q (Mg, N): group along columns of x / rows of q
+                xs = x_dev[:, prev:e].float().abs().amax(dim=1)
+                qs = qm[prev:e].amax(dim=0)
+            nz = xs >= 1e-12
+            assert bool((qs[nz] == 0x7E).all())
+        prev = e
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_small_workloads_full(gq, idx):
+    case = synth.workload(idx)
+    check_colwise(gq, case)
+
+
+@pytest.mark.parametrize("n_groups", [4, 8, 16])
+def test_colwise_large(gq, n_groups):
+    case = synth.workload(3, n_groups)
+    x = dev_bf16(case.x)
+    offs = dev_i32(case.offs)
+    q, s = gq.colwise(x, offs)
+    gq.check_device_error()
+    rng = np.random.default_rng(100 + n_groups)
+    cols = _sample(rng, case.x.shape[1], 128, 64)
+    rq, rs = oracle.colwise(case.x[:, cols], case.offs)
+    cols_d = torch.from_numpy(cols).cuda()
+    gq_q = q.view(torch.uint8).index_select(1, cols_d).cpu().numpy()
+    gq_s = s.index_select(1, cols_d).cpu().numpy()
+    assert_same(gq_q, gq_s, rq, rs, case.name)
+    _max_code_property(q, x, case.offs, 0)
+
+
+@pytest.mark.parametrize("idx,n_groups", [(4, 16), (5, 1), (5, 64)])
+def test_rowwise_large(gq, idx, n_groups):
+    case = synth.workload(idx, n_groups)
+    a = dev_bf16(case.x)
+    offs = dev_i32(case.offs)
+    qt, s = gq.rowwise_t(a, offs)
+    gq.check_device_error()
+    rng = np.random.default_rng(200 + n_groups)
+    rows = _sample(rng, case.x.shape[0], 128, 64)
+    rq, rs = oracle.rowwise_t(case.x[rows], case.offs)
+    rows_d = torch.from_numpy(rows).cuda()
+    gq_q = qt.view(torch.uint8).index_select(1, rows_d).cpu().numpy()
+    gq_s = s.index_select(0, rows_d).cpu().numpy()
+    assert_same(gq_q, gq_s, rq, rs, case.name)
+    _max_code_property(qt, a, case.offs, 1)
+    # the transpose identity at full size: rowwise_t(A) == colwise(A^T)
+    qc, sc = gq.colwise(a.t().contiguous(), offs)
+    gq.check_device_error()
+    assert torch.equal(qt.view(torch.uint8), qc.view(torch.uint8))
+    assert torch.equal(s, sc.t())

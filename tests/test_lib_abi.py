@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol
+the header declares, and rejects bad arguments on the host before touching
+CUDA (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gq_fp8.h")
+
+
+@pytest.fixture(scope="module")
+def gq():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import fp8_quantization_moe_gb300 as m
+
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for need in ("gq_fp8_colwise", "gq_fp8_rowwise_t", "gq_workspace_bytes",
+                 "gq_check_device_error", "gq_status_string"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(gq):
+    lib = ctypes.CDLL(gq.library_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    from fp8_quantization_moe_gb300 import _binding
+    assert set(_binding.SIGNATURES) == set(declared_functions())
+
+
+def test_constants_match_header(gq):
+    text = open(HEADER).read()
+    assert f"#define GQ_MAX_GROUPS {gq.GQ_MAX_GROUPS}" in text
+    assert f"#define GQ_KIND_COLWISE {gq.GQ_KIND_COLWISE}" in text
+    assert f"#define GQ_KIND_ROWWISE_T {gq.GQ_KIND_ROWWISE_T}" in text
+
+
+def test_status_strings(gq):
+    assert gq.status_string(0) == "ok"
+    assert gq.status_string(4) == "device wait timed out"
+    assert gq.version() >= 100
+
+
+def test_workspace_bytes(gq):
+    # colwise 65536x4096, 16 groups: 256 B header + 32 slab counters (256 B)
+    # + 16*4096 amax words
+    assert gq.workspace_bytes(0, 65536, 4096, 16) == 256 + 256 + 16 * 4096 * 4
+    # rowwise_t 8192x16640, 64 groups: 64 band counters + 8192*64 amax words
+    assert gq.workspace_bytes(1, 8192, 16640, 64) == 256 + 256 + 8192 * 64 * 4
+    assert gq.workspace_bytes(0, 0, 4096, 4) == 0
+    assert gq.workspace_bytes(1, 16, 0, 4) == 0
+    assert gq.workspace_bytes(0, 16, 16, 0) == 0
+    assert gq.workspace_bytes(0, 16, 16, gq.GQ_MAX_GROUPS + 1) == 0
+    assert gq.workspace_bytes(7, 16, 16, 1) == 0
+
+
+# Fake device addresses: the host-side checks return before any CUDA call,
+# so these are never dereferenced.
+A16 = 0x10000
+BAD = 0x10008
+
+
+@pytest.mark.parametrize("args,status", [
+    # x, M, K, offs, G, out, scales, ws, ws_bytes
+    ((A16, -1, 16, A16, 1, A16, A16, A16, 1 << 20), 1),
+    ((A16, 16, 16, None, 1, A16, A16, A16, 1 << 20), 1),
+    ((A16, 16, 16, A16, 0, A16, A16, A16, 1 << 20), 1),
+    ((A16, 16, 16, A16, 1025, A16, A16, A16, 1 << 20), 2),
+    ((None, 16, 16, A16, 1, A16, A16, A16, 1 << 20), 1),
+    ((BAD, 16, 16, A16, 1, A16, A16, A16, 1 << 20), 1),
+    ((A16, 16, 16, A16, 1, BAD, A16, A16, 1 << 20), 1),
+    ((A16, 16, 24, A16, 1, A16, A16, A16, 1 << 20), 2),
+    ((A16, 16, 16, A16, 1, A16, None, A16, 1 << 20), 1),
+    ((A16, 16, 16, A16, 1, A16, A16, None, 0), 1),
+    ((A16, 16, 16, A16, 1, A16, A16, A16, 16), 1),
+    ((A16, 16, 16, A16, 1, A16, A16, A16 + 16, 1 << 20), 1),
+    ((A16, 1 << 31, 16, A16, 1, A16, A16, A16, 1 << 40), 2),
+])
+def test_colwise_host_validation(gq, args, status):
+    lib = gq.lib()
+    assert lib.gq_fp8_colwise(*args, None) == status
+    assert lib.gq_last_error() != b""
+
+
+@pytest.mark.parametrize("args,status", [
+    # a, N, Mg, offs, G, out_t, scales, ws, ws_bytes
+    ((A16, 24, 64, A16, 1, A16, A16, A16, 1 << 20), 2),   # N % 16
+    ((A16, 16, 20, A16, 1, A16, A16, A16, 1 << 20), 2),   # Mg % 8
+    ((A16, 16, 64, A16, 1, A16, BAD + 2, A16, 1 << 20), 1),
+    ((A16, -16, 64, A16, 1, A16, A16, A16, 1 << 20), 1),
+    ((A16, 16, 64, A16, 1, None, A16, A16, 1 << 20), 1),
+    ((A16, 16, 64, A16, 1, A16, A16, A16, 100), 1),
+])
+def test_rowwise_host_validation(gq, args, status):
+    lib = gq.lib()
+    assert lib.gq_fp8_rowwise_t(*args, None) == status
+
+
+def test_debug_set_rejects_negative_timeout(gq):
+    assert gq.lib().gq_debug_set(0, -1) == 1
+    assert gq.lib().gq_debug_set(0, 0) == 0
+
+
+def test_binding_rejects_cpu_tensors(gq):
+    import torch
+    x = torch.zeros((16, 16), dtype=torch.bfloat16)
+    o = torch.tensor([16], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        gq.colwise(x, o)
+    with pytest.raises(ValueError):
+        gq.rowwise_t(x, o)
