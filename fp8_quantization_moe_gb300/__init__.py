@@ -14,6 +14,7 @@ supplies device memory and streams.  ``synth`` draws seeded inputs.
 """
 from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
                        GQError, check_device_error, colwise, colwise_host,
+                       colwise_noalloc,
                        debug_set, lib, library_path, rowwise_t,
                        rowwise_t_host, status_string, version,
                        workspace_bytes)
@@ -21,7 +22,8 @@ from ._build import build
 
 __all__ = [
     "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQError",
-    "build", "check_device_error", "colwise", "colwise_host", "debug_set",
+    "build", "check_device_error", "colwise", "colwise_host",
+    "colwise_noalloc", "debug_set",
     "lib", "library_path", "rowwise_t", "rowwise_t_host", "status_string",
     "version", "workspace_bytes",
 ]

@@ -30,6 +30,7 @@ SIGNATURES = {
     "gq_workspace_bytes": (_SZ, [ctypes.c_int, _I64, _I64, _I32]),
     "gq_fp8_colwise": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "gq_fp8_rowwise_t": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "gq_fp8_colwise_noalloc": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P]),
     "gq_check_device_error": (ctypes.c_int, [_P]),
     "gq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gq_last_error": (ctypes.c_char_p, []),
@@ -207,6 +208,34 @@ def rowwise_t(a: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
         st = lib().gq_fp8_rowwise_t(_ptr(a), N, Mg, _ptr(offs), G, _ptr(out),
                                     _ptr(scales), wp, wn, sh)
     _check(st, "gq_fp8_rowwise_t")
+    return out, scales
+
+
+def colwise_noalloc(x: torch.Tensor, offs: torch.Tensor, *, out=None,
+                    scales=None, stream=None):
+    """colwise() for callers that cannot allocate device memory: the library
+    uses its own fixed scratch array instead of a workspace.  Limited to
+    problems whose workspace would fit GQ_NOALLOC_SCRATCH_BYTES; calls that
+    may overlap on the GPU must not be issued (they share the scratch).
+    The outputs must be passed in by such callers; when omitted, torch
+    allocates them here as a convenience."""
+    _check_in(x, offs, "colwise_noalloc")
+    M, K = x.shape
+    G = offs.numel()
+    dev = x.device
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    if scales is None:
+        scales = torch.empty((G, K), dtype=torch.float32, device=dev)
+    if out.shape != (M, K) or out.element_size() != 1 or not out.is_contiguous():
+        raise ValueError("colwise_noalloc: out must be a contiguous 1-byte (M, K) tensor")
+    if scales.shape != (G, K) or scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError("colwise_noalloc: scales must be a contiguous float32 (G, K) tensor")
+    sh = _stream_handle(stream, dev)
+    with torch.cuda.device(dev):
+        st = lib().gq_fp8_colwise_noalloc(_ptr(x), M, K, _ptr(offs), G,
+                                          _ptr(out), _ptr(scales), sh)
+    _check(st, "gq_fp8_colwise_noalloc")
     return out, scales
 
 

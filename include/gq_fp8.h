@@ -133,6 +133,35 @@ gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,
                            size_t workspace_bytes, gq_stream_t stream);
 
 /*
+ * Colwise scaling with no allocation at all, not even a caller workspace.
+ * The pytorch/ao pages have no counterpart to this entry point; it exists for
+ * callers that cannot obtain device memory at the point where they quantize
+ * -- a plugin running inside another runtime that owns the whole device heap
+ * and lends out no workspace, or a hot path that must not call
+ * cudaMalloc / cudaFree because those can synchronise the device.
+ *
+ * Arguments, layouts and results are those of gq_fp8_colwise without the
+ * workspace.  The scratch lives in one fixed array of
+ * GQ_NOALLOC_SCRATCH_BYTES inside the library's device memory, present on
+ * every GPU that loads the library until the process exits.
+ *   - Limit: gq_workspace_bytes(GQ_KIND_COLWISE, M, K, n_groups) must be at
+ *     most GQ_NOALLOC_SCRATCH_BYTES (about n_groups * K <= 261,900);
+ *     larger calls return GQ_ERR_UNSUPPORTED before enqueueing anything.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, that device current); make that first call
+ *     before any stream capture.
+ *   - Each call clears the part of the array it uses (cudaMemsetAsync on
+ *     `stream`), so leftovers of an earlier call do not matter.
+ *   - All calls on a device share the array: calls whose GPU work may
+ *     overlap (other streams, other host threads) race and corrupt each
+ *     other's results.  Issue them on one stream, or order them.
+ */
+#define GQ_NOALLOC_SCRATCH_BYTES (1u << 20)
+gq_status gq_fp8_colwise_noalloc(const void* x, int64_t M, int64_t K,
+                                 const int32_t* offs, int32_t n_groups,
+                                 void* out, float* scales, gq_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns GQ_ERR_TIMEOUT if any kernel since the last check gave up a
  * bounded wait, GQ_ERR_CUDA if the stream reports an error, else GQ_OK.
