@@ -287,8 +287,8 @@ def run_mine(args):
     M, K, G = COLWISE_SHAPE
     N, Mg, Gr = ROWWISE_SHAPE
     seed_off = 7919 * rank  # each rank its own batch
-    c = synth.colwise_large(G, seed=1300 + G + seed_off)
-    r = synth.rowwise_outliers(Gr, seed=1500 + Gr + seed_off)
+    c = synth.colwise_large(G, seed=1300 + G + seed_off, rows=M, cols=K)
+    r = synth.rowwise_outliers(Gr, seed=1500 + Gr + seed_off, N=N, Mg=Mg)
 
     def to_dev(bits):
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -408,10 +408,10 @@ def run_mine(args):
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16->e4m3 (fp32 scale math)", "data": "synthetic (seeded)",
         "config": {
-            "workload": "colwise X 65536x4096 bf16, 16 groups (rows scaled "
-                        "10^U(-2,2)) + rowwise_t A 8192x16640 bf16, 64 groups "
+            "workload": f"colwise X {M}x{K} bf16, {G} groups (rows scaled "
+                        f"10^U(-2,2)) + rowwise_t A {N}x{Mg} bf16, {Gr} groups "
                         "(2 empty, 0.5% outlier columns x1000)",
-            "global_batch": 65536 + 16640, "parallelism": f"replicas x{world}",
+            "global_batch": M + Mg, "parallelism": f"replicas x{world}",
             "l2": "inputs (512 MB, 272 MB) larger than L2 and disjoint; no flush",
         },
         "per_call": {
@@ -461,7 +461,15 @@ def main(argv=None):
     ap.add_argument("--clock-window", type=float, default=1.5,
                     help="seconds of sustained load around the timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--half", action="store_true",
+                    help="profiling case: half the tokens of each workload "
+                         "(inputs 256 MB and 136 MB, still larger than L2); "
+                         "not the benchmark configuration")
     args = ap.parse_args(argv)
+    if args.half:
+        global COLWISE_SHAPE, ROWWISE_SHAPE
+        COLWISE_SHAPE = (COLWISE_SHAPE[0] // 2,) + COLWISE_SHAPE[1:]
+        ROWWISE_SHAPE = (ROWWISE_SHAPE[0], ROWWISE_SHAPE[1] // 2, ROWWISE_SHAPE[2])
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least three warm-up steps
     if args.impl == "reference":

@@ -16,7 +16,7 @@ from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
                        GQError, check_device_error, colwise, colwise_host,
                        colwise_noalloc,
                        debug_set, lib, library_path, rowwise_t,
-                       rowwise_t_host, status_string, version,
+                       rowwise_t_host, set_lag, status_string, version,
                        workspace_bytes)
 from ._build import build
 
@@ -24,6 +24,7 @@ __all__ = [
     "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQError",
     "build", "check_device_error", "colwise", "colwise_host",
     "colwise_noalloc", "debug_set",
-    "lib", "library_path", "rowwise_t", "rowwise_t_host", "status_string",
+    "lib", "library_path", "rowwise_t", "rowwise_t_host", "set_lag",
+    "status_string",
     "version", "workspace_bytes",
 ]

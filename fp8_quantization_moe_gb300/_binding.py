@@ -36,6 +36,7 @@ SIGNATURES = {
     "gq_last_error": (ctypes.c_char_p, []),
     "gq_version": (ctypes.c_int, []),
     "gq_debug_set": (ctypes.c_int, [ctypes.c_int, _I64]),
+    "gq_set_lag": (ctypes.c_int, [ctypes.c_int, ctypes.c_int32]),
 }
 
 
@@ -252,6 +253,11 @@ def debug_set(skip_arrival: bool = False, wait_timeout_ns: int = 0):
     """Test hook: see gq_debug_set in include/gq_fp8.h."""
     _check(lib().gq_debug_set(int(bool(skip_arrival)), int(wait_timeout_ns)),
            "gq_debug_set")
+
+
+def set_lag(kind: int, lag: int = 0):
+    """Tuning knob: see gq_set_lag in include/gq_fp8.h (0 = automatic)."""
+    _check(lib().gq_set_lag(int(kind), int(lag)), "gq_set_lag")
 
 
 # ------------------------------------------------------ host-buffer calls --

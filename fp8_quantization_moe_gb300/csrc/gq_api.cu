@@ -139,6 +139,18 @@ gq_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype,
   return GQ_OK;
 }
 
+int32_t schedule_lag(int32_t forced, int64_t units, int64_t groups,
+                     int64_t grid, int stages) {
+  // Phase B of group d starts 2 * lag * units tickets after the last phase-A
+  // ticket of d; the producers run up to stages * grid tickets ahead of the
+  // consumers, and CTAs drift apart by about grid more.
+  int64_t lag = forced > 0 ? forced
+                           : ((stages + 2) * grid + 2 * units - 1) / (2 * units);
+  if (lag < 1) lag = 1;
+  if (lag > groups) lag = groups;
+  return static_cast<int32_t>(lag);
+}
+
 WorkspaceLayout workspace_layout(int64_t dep_groups, int64_t amax_words) {
   auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
   WorkspaceLayout L;
@@ -324,6 +336,14 @@ const char* gq_status_string(gq_status status) {
 const char* gq_last_error(void) { return g_msg; }
 
 int gq_version(void) { return 100; }
+
+gq_status gq_set_lag(int kind, int32_t lag) {
+  if (kind != GQ_KIND_COLWISE && kind != GQ_KIND_ROWWISE_T)
+    return fail(GQ_ERR_INVALID_ARG, "gq_set_lag: unknown kind %d", kind);
+  if (lag < 0) return fail(GQ_ERR_INVALID_ARG, "gq_set_lag: negative lag");
+  g_dbg.lag[kind] = lag;
+  return GQ_OK;
+}
 
 gq_status gq_debug_set(int skip_arrival, int64_t wait_timeout_ns) {
   if (wait_timeout_ns < 0)

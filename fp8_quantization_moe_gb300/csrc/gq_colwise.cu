@@ -4,50 +4,58 @@
 // per (group, column).  This is the per-token-group scaling "along dim0" of
 // pytorch/ao #2668 ("use smaller block sizes for per group scaling kernels
 // to improve perf", intro); the page's lesson -- the grid was too small to
-// fill the SMs -- is answered here by a persistent grid sized to the SM
-// count that claims 16 KB tiles one by one.
+// fill the SMs -- is answered here by a persistent grid of two CTAs per SM
+// that works through 16 KB tiles.
 //
-// Tiles are kR = 64 rows x kW = 128 columns (256-byte row runs), loaded by
-// TMA into a kStages-deep shared-memory ring.  A column slab (all M rows of
-// kW columns) is one dependency group: phase B of a tile of slab d needs the
-// amax of every tile of slab d.  See gq_device.cuh for the schedule.
+// Tiles are kR = 64 rows x kW = 128 columns, loaded by TMA as two 64-column
+// halves with the 128-byte swizzle (row r of a half is 128 bytes; its
+// 16-byte chunk k sits at slot k ^ (r % 8)), into a kStages-deep ring.  A
+// column slab (all M rows of kW columns) is one dependency group: phase B of
+// a tile of slab d needs the amax of every tile of slab d.  See
+// gq_device.cuh for the schedule.  In phase B the producer lanes bring the
+// 128 amax words of each of the tile's first kSegA segments into the stage
+// (one 16-byte cp.async per lane).
 //
-// Per tile, phase A: each consumer thread owns one 16-byte column chunk
-// (8 columns) and every 8th row; it folds |x| with max.xorsign.abs.bf16x2,
-// the CTA reduces over rows through shared memory, and one atomicMax per
-// (group, column) goes to the amax words.  Phase B: the scale of each
-// (group, column) is 448 / max(amax, 1e-12) (IEEE division), the product
-// x * scale is an fp32 multiply, and cvt.rn.satfinite.e4m3x2 packs pairs;
-// 8 output bytes per thread and row leave as one 8-byte store, so a warp
-// writes two 128-byte row runs.
-#include <cstdio>
-
+// The eight consumer warps work on each stage independently -- no barrier
+// among them inside the loop:
+//   phase A: warp w takes a 16-column strip (half w / 4, chunks 2 (w % 4)
+//     and 2 (w % 4) + 1); a lane folds |x| of its chunk over every 16th row
+//     with max.xorsign.abs.bf16x2, a butterfly over the 16 lanes of a chunk
+//     finishes the column maxima, and 16 lanes issue one atomicMax each;
+//   phase B: warp w takes rows 8w .. 8w + 7; a lane computes four of the
+//     128 scales (448 / max(amax, 1e-12), IEEE division) and gathers the
+//     eight of its chunk by shuffles; products are IEEE fp32 multiplies
+//     (mul.rn.f32x2), packed with cvt.rn.satfinite.e4m3x2; each warp store
+//     writes two 128-byte output row runs.
 #include "gq_device.cuh"
 #include "gq_internal.h"
 
 namespace gq {
 namespace colwise {
 
-constexpr int kStages = 6;
-constexpr int kConsumerWarps = 4;
+constexpr int kStages = 5;
+constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
-constexpr int kTileBytes = kW * kR * 2;
-constexpr int kChunks = kW / 8;  // 16-byte column chunks per tile row
-static_assert(kConsumers == kW, "one consumer thread per column in the reduction");
-static_assert(kConsumers == kChunks * (kR / 8), "one 16-byte chunk and every 8th row per thread");
+constexpr int kThreads = kConsumers + 64;  // + producer warp + signal warp
+constexpr int kSigSlots = 16;
+constexpr int kHalfBytes = 64 * kR * 2;  // one swizzled 64-column half
+constexpr int kTileBytes = 2 * kHalfBytes;
+constexpr int kSegA = 4;  // segments whose amax words ride in the stage
+static_assert(kW == 128 && kR == 64, "tile shape assumed by the lane maps");
+static_assert(kW == 32 * 4, "one 16-byte amax chunk per producer lane");
+static_assert(kSigSlots > kStages, "a warp cannot lap the signal ring");
 
 using Hdr = TileHdr<kR>;
 
 struct Smem {
   uint8_t tile[kStages][kTileBytes];  // first member: 1024-byte aligned
+  alignas(16) uint32_t amax[kStages][kSegA][kW];  // phase B amax words
   Hdr hdr[kStages];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t ends_ready;
+  SigRing<kSigSlots> sig;
   int32_t ends[kMaxGroups];
-  uint32_t red[kConsumerWarps][kChunks * 4];
-  alignas(16) float sc[2][kW];
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
@@ -56,9 +64,8 @@ struct Params {
   const int32_t* offs;
   uint8_t* out;
   float* scales;
-  uint32_t* ticket;  // one word
-  uint32_t* done;    // one word per slab
-  uint32_t* amax;    // (G, K) fp32 bit patterns
+  uint32_t* done;  // one word per slab
+  uint32_t* amax;  // (G, K) fp32 bit patterns
   unsigned* err;
   int32_t M, K, G;
   Schedule sched;
@@ -66,39 +73,78 @@ struct Params {
   int32_t skip_arrival;
 };
 
+// Shared-memory address of chunk `k` (0..15, 8 columns each) of tile row r.
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t tile, int r, int k) {
+  return tile + static_cast<uint32_t>((k >> 3) * kHalfBytes + r * 128 +
+                                      (((k ^ r) & 7) << 4));
+}
+
+// The producer warp: group-end table, then per ticket header + loads.
 __device__ __forceinline__ void producer(Smem& s, const CUtensorMap* xmap,
-                                         const Params& p) {
+                                         const Params& p, int lane) {
+  build_ends(p.offs, p.G, p.M, s.ends, lane);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&s.ends_ready);
+
   const uint64_t pol_a = policy_evict_last();
   const uint64_t pol_b = policy_evict_first();
-  const uint32_t total = 2u * static_cast<uint32_t>(p.sched.units) *
-                         static_cast<uint32_t>(p.sched.groups);
-  bool ends_ok = false;
+  const int32_t units = p.sched.units;
+  const int32_t blocks = 2 * p.sched.groups;
+  int32_t ready_dg = -1;  // slabs <= ready_dg are complete
   int st = 0;
   uint32_t ph = 0;
-  for (;;) {
-    if (!mbar_wait(&s.empty[st], ph ^ 1u, 4 * p.timeout_ns, p.err)) return;
-    const uint32_t t = atomicAdd(p.ticket, 1u);
+  for (TicketWalk tw(blockIdx.x, gridDim.x, units);; tw.next(units)) {
     Hdr& h = s.hdr[st];
-    if (t >= total) {
-      h.phase = -1;
-      mbar_arrive(&s.full[st]);
+    if (!mbar_wait(&s.empty[st], ph ^ 1u, 4 * p.timeout_ns, p.err)) return;
+    bool stop = tw.block >= blocks;
+    int32_t phase = 0, dg = 0;
+    if (!stop) decode_block(tw.block, p.sched, phase, dg);
+    if (!stop && phase == 1 && dg > ready_dg) {
+      bool ok = true;
+      if (lane == 0)
+        ok = wait_counter(p.done + dg, static_cast<uint32_t>(units), p.timeout_ns,
+                          p.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok) {
+        ld_acquire_u32(p.done + dg);  // every lane acquires before reading amax
+        ready_dg = dg;
+      }
+      stop = !ok;
+    }
+    if (stop) {
+      if (lane == 0) {
+        h.phase = -1;
+        mbar_arrive(&s.full[st]);
+      }
       return;
     }
-    const Ticket k = decode_ticket(t, p.sched);
-    const int32_t c0 = k.dg * kW;
-    const int32_t r0 = k.unit * kR;
-    mbar_expect_tx(&s.full[st], kTileBytes);
-    tma_load_2d(s.tile[st], xmap, c0, r0, &s.full[st],
-                k.phase == 0 ? pol_a : pol_b);
-    if (!ends_ok) {
-      if (!mbar_wait(&s.ends_ready, 0u, 4 * p.timeout_ns, p.err)) return;
-      ends_ok = true;
+    const int32_t c0 = dg * kW;
+    const int32_t r0 = tw.unit * kR;
+    build_header_warp(h, s.ends, p.G, r0, min(r0 + kR, p.M), tw.unit == units - 1,
+                      lane);
+    __syncwarp();
+    if (phase == 1) {
+      const int n = min(static_cast<int>(h.nseg), kSegA);
+      const int32_t col = c0 + 4 * lane;
+      for (int j = 0; j < n; ++j)
+        cp_async_16(smem_addr(&s.amax[st][j][4 * lane]),
+                    p.amax + static_cast<size_t>(h.seg_g[j]) * p.K + (col < p.K ? col : 0),
+                    col < p.K ? 16u : 0u);
+      cp_async_mbar_arrive(&s.full[st]);
     }
-    h.phase = k.phase;
-    h.dg = k.dg;
-    fill_segments(h, s.ends, p.G, r0, min(r0 + kR, p.M),
-                  k.unit == p.sched.units - 1);
-    mbar_arrive(&s.full[st]);
+    if (lane == 0) {
+      h.phase = phase;
+      h.dg = dg;
+      h.unit = tw.unit;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const bool two = c0 + 64 < p.K;  // the second half holds columns
+      const uint64_t pol = phase == 0 ? pol_a : pol_b;
+      mbar_arrive_expect_tx(&s.full[st], two ? kTileBytes : kHalfBytes);
+      tma_load_2d(s.tile[st], xmap, c0, r0, &s.full[st], pol);
+      if (two) tma_load_2d(s.tile[st] + kHalfBytes, xmap, c0 + 64, r0, &s.full[st], pol);
+    }
     if (++st == kStages) {
       st = 0;
       ph ^= 1u;
@@ -106,124 +152,111 @@ __device__ __forceinline__ void producer(Smem& s, const CUtensorMap* xmap,
   }
 }
 
-// Phase A: fold |x| of the tile into the amax words of each segment.
+// Phase A, warp w: column maxima of its 16-column strip for each segment,
+// one atomicMax per (segment, column); then the tile goes to the signal lane.
 __device__ __forceinline__ void phase_a(Smem& s, const Hdr& h, uint32_t tile,
-                                        const Params& p, int t, int warp,
-                                        int lane) {
-  const int cc = t & (kChunks - 1);  // column chunk
-  const int rl = t / kChunks;        // row lane: rows rl, rl + 8, ...
-  const int32_t c0 = h.dg * kW;
+                                        const Params& p, int warp, int lane,
+                                        uint32_t& sig_seq) {
+  const int k = (warp >> 2) * 8 + (warp & 3) * 2 + (lane & 1);  // chunk 0..15
+  const int r0 = lane >> 1;                                      // rows r0 + 16 i
+  const int32_t col = h.dg * kW + 8 * k + ((lane >> 1) & 7);    // RED column
   const int nseg = h.nseg;
   for (int j = 0; j < nseg; ++j) {
     const int a = h.seg_lo[j], b = h.seg_hi[j];
     uint32_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-    if (a == 0 && b == kR) {
 #pragma unroll
-      for (int i = 0; i < kR / 8; ++i) {
-        const int r = rl + 8 * i;
-        const uint4 v = lds128(tile + (r * kW + cc * 8) * 2);
+    for (int i = 0; i < kR / 16; ++i) {
+      const int r = r0 + 16 * i;
+      if (r >= a && r < b) {
+        const uint4 v = lds128(chunk_addr(tile, r, k));
         acc0 = absmax_bf16x2(acc0, v.x);
         acc1 = absmax_bf16x2(acc1, v.y);
         acc2 = absmax_bf16x2(acc2, v.z);
         acc3 = absmax_bf16x2(acc3, v.w);
       }
-    } else {
-#pragma unroll 4
-      for (int i = 0; i < kR / 8; ++i) {
-        const int r = rl + 8 * i;
-        if (r >= a && r < b) {
-          const uint4 v = lds128(tile + (r * kW + cc * 8) * 2);
-          acc0 = absmax_bf16x2(acc0, v.x);
-          acc1 = absmax_bf16x2(acc1, v.y);
-          acc2 = absmax_bf16x2(acc2, v.z);
-          acc3 = absmax_bf16x2(acc3, v.w);
-        }
-      }
     }
-    // lanes l and l ^ 16 hold the same column chunk
-    acc0 = absmax_bf16x2(acc0, __shfl_xor_sync(0xffffffffu, acc0, 16));
-    acc1 = absmax_bf16x2(acc1, __shfl_xor_sync(0xffffffffu, acc1, 16));
-    acc2 = absmax_bf16x2(acc2, __shfl_xor_sync(0xffffffffu, acc2, 16));
-    acc3 = absmax_bf16x2(acc3, __shfl_xor_sync(0xffffffffu, acc3, 16));
-    if (lane < 16) {
-      uint32_t* r = &s.red[warp][lane * 4];
-      r[0] = acc0;
-      r[1] = acc1;
-      r[2] = acc2;
-      r[3] = acc3;
-    }
-    named_bar(1, kConsumers);
-    {
-      // thread t -> column t of the slab
-      const int word = t >> 1;  // chunk * 4 + word-in-chunk
-      const int shift = (t & 1) * 16;
-      uint32_t m = 0;
+    // lanes of equal parity hold the same chunk
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const uint32_t v = (s.red[w][word] >> shift) & 0x7FFFu;
-        m = v > m ? v : m;
-      }
-      const int32_t col = c0 + t;
+    for (int x = 2; x < 32; x <<= 1) {
+      acc0 = absmax_bf16x2(acc0, __shfl_xor_sync(0xffffffffu, acc0, x));
+      acc1 = absmax_bf16x2(acc1, __shfl_xor_sync(0xffffffffu, acc1, x));
+      acc2 = absmax_bf16x2(acc2, __shfl_xor_sync(0xffffffffu, acc2, x));
+      acc3 = absmax_bf16x2(acc3, __shfl_xor_sync(0xffffffffu, acc3, x));
+    }
+    if (lane < 16) {
+      const int c = lane >> 1;  // column within the chunk
+      const uint32_t w = c < 2 ? acc0 : c < 4 ? acc1 : c < 6 ? acc2 : acc3;
+      const uint32_t m = ((c & 1) ? (w >> 16) : w) & 0x7FFFu;
       if (m != 0u && col < p.K)
         atomicMax(p.amax + static_cast<size_t>(h.seg_g[j]) * p.K + col, m << 16);
     }
-    named_bar(1, kConsumers);
   }
-  if (t == 0) {
-    const bool skip = p.skip_arrival && h.dg == 0 && h.lo == 0;
-    __threadfence();
-    if (!skip) atomicAdd(p.done + h.dg, 1u);
-  }
+  sig_post(s.sig, (p.skip_arrival && h.dg == 0 && h.unit == 0) ? kSigSkip : h.dg,
+           warp * 32 + lane, lane, sig_seq, 4 * p.timeout_ns, p.err);
 }
 
-// Phase B: scales, then the scaled cast of every row inside a group.
-__device__ __forceinline__ void phase_b(Smem& s, const Hdr& h, uint32_t tile,
-                                        const Params& p, int t,
-                                        uint32_t& sc_seq) {
-  const int cc = t & (kChunks - 1);
-  const int rl = t / kChunks;
+// Phase B, warp w: rows 8w .. 8w + 7 of the tile, all 128 columns.
+__device__ __forceinline__ void phase_b(Smem& s, const Hdr& h, int st,
+                                        uint32_t tile, const Params& p,
+                                        int warp, int lane) {
   const int32_t c0 = h.dg * kW;
-  if (t == 0)
-    wait_counter(p.done + h.dg, static_cast<uint32_t>(p.sched.units),
-                 p.timeout_ns, p.err);
-  named_bar(1, kConsumers);
-  const int32_t col = c0 + t;
-  const bool col_in = col < p.K;
-  for (int g = h.own_lo; g < h.own_hi; ++g) {
-    if (col_in) {
-      const size_t i = static_cast<size_t>(g) * p.K + col;
-      p.scales[i] = scale_from_amax_bits(ld_cg_u32(p.amax + i));
+  const int k = lane & 15;  // chunk: columns 8k .. 8k + 7
+  const bool chunk_in = c0 + 8 * k < p.K;
+  const int32_t c4 = c0 + 4 * lane;  // this lane's four scale columns
+  const bool c4_in = c4 < p.K;
+  const int rb = 8 * warp + (lane >> 4);  // this lane's rows: rb + 2 i
+  // owned groups without rows: amax 0
+  if (warp == 0) {
+    for (int g = h.own_lo; g < h.own_hi; ++g) {
+      const int32_t gs = g ? s.ends[g - 1] : 0;
+      if (c4_in && s.ends[g] == gs) {
+        const float e = scale_from_amax_bits(0u);
+        *reinterpret_cast<float4*>(p.scales + static_cast<size_t>(g) * p.K + c4) =
+            make_float4(e, e, e, e);
+      }
     }
   }
-  const bool chunk_in = c0 + cc * 8 < p.K;
   const int nseg = h.nseg;
   for (int j = 0; j < nseg; ++j) {
     const int a = h.seg_lo[j], b = h.seg_hi[j];
-    float* scb = s.sc[sc_seq & 1u];
-    ++sc_seq;
-    scb[t] = col_in ? scale_from_amax_bits(ld_cg_u32(
-                          p.amax + static_cast<size_t>(h.seg_g[j]) * p.K + col))
-                    : 0.0f;
-    named_bar(1, kConsumers);
-    const float4 sa = *reinterpret_cast<const float4*>(scb + cc * 8);
-    const float4 sb = *reinterpret_cast<const float4*>(scb + cc * 8 + 4);
-    uint8_t* obase =
-        p.out + static_cast<size_t>(h.lo) * p.K + static_cast<size_t>(c0 + cc * 8);
-#pragma unroll 4
-    for (int i = 0; i < kR / 8; ++i) {
-      const int r = rl + 8 * i;
+    if (8 * warp + 7 < a || 8 * warp >= b) continue;  // no row of this warp
+    const int g = h.seg_g[j];
+    uint4 am;
+    if (j < kSegA) {
+      am = *reinterpret_cast<const uint4*>(&s.amax[st][j][4 * lane]);
+    } else if (c4_in) {
+      const uint32_t* src = p.amax + static_cast<size_t>(g) * p.K + c4;
+      am = make_uint4(ld_cg_u32(src), ld_cg_u32(src + 1), ld_cg_u32(src + 2),
+                      ld_cg_u32(src + 3));
+    } else {
+      am = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const float s0 = scale_from_amax_bits(am.x), s1 = scale_from_amax_bits(am.y);
+    const float s2 = scale_from_amax_bits(am.z), s3 = scale_from_amax_bits(am.w);
+    // the group starts inside the tile at row a: the warp holding row a
+    // writes its scales
+    if (warp == (a >> 3) && c4_in && g >= h.own_lo && g < h.own_hi)
+      *reinterpret_cast<float4*>(p.scales + static_cast<size_t>(g) * p.K + c4) =
+          make_float4(s0, s1, s2, s3);
+    float sc[8];
+    {
+      const int l0 = 2 * k, l1 = 2 * k + 1;  // lanes holding columns 8k..8k+7
+      sc[0] = __shfl_sync(0xffffffffu, s0, l0);
+      sc[1] = __shfl_sync(0xffffffffu, s1, l0);
+      sc[2] = __shfl_sync(0xffffffffu, s2, l0);
+      sc[3] = __shfl_sync(0xffffffffu, s3, l0);
+      sc[4] = __shfl_sync(0xffffffffu, s0, l1);
+      sc[5] = __shfl_sync(0xffffffffu, s1, l1);
+      sc[6] = __shfl_sync(0xffffffffu, s2, l1);
+      sc[7] = __shfl_sync(0xffffffffu, s3, l1);
+    }
+    uint8_t* obase = p.out + static_cast<size_t>(h.lo) * p.K + static_cast<size_t>(c0 + 8 * k);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = rb + 2 * i;
       if (r >= a && r < b && chunk_in) {
-        const uint4 v = lds128(tile + (r * kW + cc * 8) * 2);
-        const uint32_t w0 =
-            cvt_e4m3x2(__fmul_rn(bf16_lo(v.x), sa.x), __fmul_rn(bf16_hi(v.x), sa.y)) |
-            (cvt_e4m3x2(__fmul_rn(bf16_lo(v.y), sa.z), __fmul_rn(bf16_hi(v.y), sa.w))
-             << 16);
-        const uint32_t w1 =
-            cvt_e4m3x2(__fmul_rn(bf16_lo(v.z), sb.x), __fmul_rn(bf16_hi(v.z), sb.y)) |
-            (cvt_e4m3x2(__fmul_rn(bf16_lo(v.w), sb.z), __fmul_rn(bf16_hi(v.w), sb.w))
-             << 16);
-        __stcs(reinterpret_cast<uint2*>(obase + static_cast<size_t>(r) * p.K),
-               make_uint2(w0, w1));
+        const uint2 o = quant8(lds128(chunk_addr(tile, r, k)), sc);
+        __stcs(reinterpret_cast<uint2*>(obase + static_cast<size_t>(r) * p.K), o);
       }
     }
   }
@@ -242,40 +275,37 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], kConsumerWarps);
     }
-    mbar_init(&s.ends_ready, 32);
+    mbar_init(&s.ends_ready, 1);
+    sig_init(s.sig, kConsumerWarps);
     fence_mbar_init();
   }
   __syncthreads();
 
+  if (warp == kConsumerWarps + 1) {
+    if (lane == 0) sig_loop(s.sig, p.done, 8 * p.timeout_ns, p.err);
+    return;
+  }
   if (warp == kConsumerWarps) {
-    if (lane == 0) {
-      prefetch_tensormap(&xmap);
-      producer(s, &xmap, p);
-    }
+    if (lane == 0) prefetch_tensormap(&xmap);
+    producer(s, &xmap, p, lane);
     return;
   }
 
-  if (warp == 0) {
-    build_ends(p.offs, p.G, p.M, s.ends, lane);
-    __syncwarp();
-    mbar_arrive(&s.ends_ready);
-  }
-
-  const int t = threadIdx.x;
+  mbar_wait(&s.ends_ready, 0u, 4 * p.timeout_ns, p.err);
   int st = 0;
   uint32_t ph = 0;
-  uint32_t sc_seq = 0;
+  uint32_t sig_seq = 0;
   for (;;) {
     const bool ok = mbar_wait(&s.full[st], ph, 4 * p.timeout_ns, p.err);
-    if (named_bar_any(1, kConsumers, !ok)) break;  // all consumers agree
+    if (__any_sync(0xffffffffu, !ok)) break;  // the warp leaves together
     const Hdr& h = s.hdr[st];
     const int phase = h.phase;
     if (phase < 0) break;
     const uint32_t tile = smem_addr(s.tile[st]);
     if (phase == 0)
-      phase_a(s, h, tile, p, t, warp, lane);
+      phase_a(s, h, tile, p, warp, lane, sig_seq);
     else
-      phase_b(s, h, tile, p, t, sc_seq);
+      phase_b(s, h, st, tile, p, warp, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[st]);
     if (++st == kStages) {
@@ -283,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       ph ^= 1u;
     }
   }
+  sig_post(s.sig, kSigEnd, warp * 32 + lane, lane, sig_seq, 4 * p.timeout_ns, p.err);
 }
 
 gq_status setup(DeviceInfo& info) {
@@ -309,8 +340,8 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   gq_status st = encode_tiled_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                  const_cast<void*>(x), static_cast<uint64_t>(K),
                                  static_cast<uint64_t>(M),
-                                 static_cast<uint64_t>(K) * 2, kW, kR,
-                                 CU_TENSOR_MAP_SWIZZLE_NONE);
+                                 static_cast<uint64_t>(K) * 2, 64, kR,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != GQ_OK) return st;
 
   Params p;
@@ -320,10 +351,8 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   const int64_t max_ctas =
       static_cast<int64_t>(info.sm_count) * info.colwise_ctas_per_sm;
   const int grid = static_cast<int>(total < max_ctas ? total : max_ctas);
-  int64_t lag = (2ll * grid + p.sched.units - 1) / p.sched.units;
-  if (lag < 1) lag = 1;
-  if (lag > p.sched.groups) lag = p.sched.groups;
-  p.sched.lag = static_cast<int32_t>(lag);
+  p.sched.lag = schedule_lag(dbg.lag[GQ_KIND_COLWISE], p.sched.units, p.sched.groups,
+                             grid, kStages);
 
   const WorkspaceLayout L =
       workspace_layout(p.sched.groups, static_cast<int64_t>(G) * K);
@@ -331,7 +360,6 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   p.offs = offs;
   p.out = static_cast<uint8_t*>(out);
   p.scales = scales;
-  p.ticket = reinterpret_cast<uint32_t*>(w);
   p.done = reinterpret_cast<uint32_t*>(w + L.counters);
   p.amax = reinterpret_cast<uint32_t*>(w + L.amax);
   p.err = info.err_word;
@@ -343,8 +371,13 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
 
   st = check_cuda(cudaMemsetAsync(ws, 0, L.total, stream), "colwise: clear workspace");
   if (st != GQ_OK) return st;
-  colwise_kernel<<<grid, kThreads, kSmemBytes, stream>>>(xmap, p);
-  return check_cuda(cudaGetLastError(), "colwise: launch");
+  // cooperative: the static ticket order needs every CTA resident
+  void* args[] = {&xmap, &p};
+  return check_cuda(
+      cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(colwise_kernel),
+                                  dim3(grid), dim3(kThreads), args, kSmemBytes,
+                                  stream),
+      "colwise: launch");
 }
 
 }  // namespace colwise

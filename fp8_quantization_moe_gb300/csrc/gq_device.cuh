@@ -1,22 +1,36 @@
 // gq_device.cuh -- device building blocks shared by the two quantization
-// kernels: inline-PTX wrappers (mbarrier, TMA, L2 policies, e4m3 convert),
-// bounded waits, the group-end table, and the ticket schedule.
+// kernels: inline-PTX wrappers (mbarrier, TMA, cp.async, L2 policies, e4m3
+// convert), bounded waits, the group-end table, tile headers and the ticket
+// schedule.
 //
-// Execution model (both kernels).  A persistent grid of CTAs, each with one
-// producer warp and kConsumerWarps consumer warps.  The work is a list of
-// tiles of the input.  A tile is visited twice: in phase A its |x| maxima
-// are folded into per-(group, column) or per-(row, group) amax words with
+// Execution model (both kernels).  A persistent grid, launched cooperatively
+// so that every CTA is resident, of CTAs with two roles: a producer warp that
+// fills a ring of shared-memory stages, and consumer warps that process each
+// stage together.  A tile is visited twice: in phase A its |x| maxima are
+// folded into per-(group, column) or per-(row, group) amax words with
 // atomicMax; in phase B, once every phase-A tile its amax words depend on is
 // done, it is re-read, scaled and cast.  Tiles that share amax words form a
 // "dependency group" (a column slab for colwise, a row band for rowwise_t).
-// Tickets are claimed with one atomicAdd per tile in a fixed order in which
-// phase A of dependency group d+L precedes phase B of group d (L = the lag),
-// so that by the time phase B of a group is claimed, its phase-A tiles are
-// long finished and its bytes still sit in L2 (loaded with evict_last):
-// HBM sees one read of the input.  Every CTA processes the tickets it claims
-// in increasing order, so the smallest unfinished ticket can always make
-// progress: the schedule cannot deadlock, even when not all CTAs are
-// resident.  The wait for a dependency group is nonetheless bounded in time.
+// Tickets follow a fixed order in which phase A of dependency group d+L
+// precedes phase B of group d (L = the lag), so that by the time phase B of a
+// group comes up its phase-A tiles are long finished and its bytes still sit
+// in L2 (loaded with evict_last): HBM sees one read of the input.  CTA c
+// takes tickets c, c + grid, c + 2 grid, ... in that order.
+//
+// For every ticket the producer warp builds the tile header (the group
+// segments inside the tile), starts the TMA load of the tile and, in phase
+// B, first waits for the dependency group to be complete and then copies the
+// amax words of the tile's first segments into the stage with cp.async, so
+// that the consumers neither wait on other CTAs nor on L2 latency for them.
+// Finished phase-A tiles leave the consumers through a small ring of
+// shared-memory slots to a signal lane, which publishes them on the groups'
+// done counters with release reductions: the memory fence that publishing
+// implies stalls that lane only, never the consumers.
+//
+// Progress: all CTAs are resident and each takes its tickets in increasing
+// order, so the smallest unfinished ticket can always advance -- its phase-A
+// dependencies have smaller tickets -- and the schedule cannot deadlock.
+// Every wait is nonetheless bounded in time.
 #pragma once
 
 #include <cuda.h>
@@ -35,19 +49,20 @@ constexpr unsigned kErrDepTimeout = 1u;   // a dependency-group wait expired
 constexpr unsigned kErrMbarTimeout = 2u;  // an mbarrier wait expired
 
 // ------------------------------------------------------------ tile header --
-// Written by the producer lane into shared memory next to each stage; read by
-// the consumers after the stage's full barrier completes.
+// Written by the producer warp into shared memory next to each stage; read by
+// the consumers after the stage's full barrier completes.  Segment bounds are
+// relative to lo and at most 255 (tiles span at most 128 tokens).
 template <int kMaxSeg>
 struct alignas(16) TileHdr {
-  int32_t phase;   // 0 = A (amax), 1 = B (scale + cast), -1 = no more work
+  int32_t phase;   // 0 = A (amax), 1 = B (scale + cast), -1 = stop
   int32_t dg;      // dependency group
   int32_t lo, hi;  // token range [lo, hi) of the tile, clamped to the extent
   int32_t own_lo, own_hi;  // groups whose scales phase B of this tile writes
   int32_t nseg;            // nonempty group segments inside [lo, hi)
-  int32_t last;            // 1 if the tile is the last of its group dim
-  int32_t seg_g[kMaxSeg];
-  int32_t seg_lo[kMaxSeg];  // relative to lo
-  int32_t seg_hi[kMaxSeg];
+  int32_t unit;            // tile within the dependency group
+  int16_t seg_g[kMaxSeg];
+  uint8_t seg_lo[kMaxSeg];
+  uint8_t seg_hi[kMaxSeg];
 };
 
 // ---------------------------------------------------------- PTX wrappers --
@@ -86,16 +101,45 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
+// Blocks for up to kSuspendNs (or until the phase completes) and reports
+// whether the phase with the given parity has completed; a waiting thread
+// sleeps instead of spinning, leaving issue slots to the working warps.
+constexpr uint32_t kSuspendNs = 100000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking probe of the same condition.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Arrival that also announces `bytes` of asynchronous transfers to come.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar,
+                                                      uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
@@ -114,6 +158,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
   }
   return true;
+}
+
+// 16-byte copy global -> shared (L2 only); reads src_bytes (0 or 16) and
+// zero-fills the rest.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src,
+                                            uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// Makes the current phase of `bar` also wait for the completion of every
+// cp.async this thread has issued (adds one pending arrival now, which the
+// copies' completion performs).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -270,28 +332,37 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   return v;
 }
 
+// Release reduction: every write that happens before it (in this thread or,
+// through synchronisation, in others) is visible to whoever acquires the
+// counter value it produces.
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_volatile_u32(const unsigned* p) {
   return *reinterpret_cast<const volatile unsigned*>(p);
 }
 
-// Waits until *counter >= target.  Bounded: after `timeout_ns` it records
-// kErrDepTimeout and returns; it also returns at once when another block has
-// already recorded an error, so one lost signal cannot stall every block for
-// the full timeout.
-__device__ __forceinline__ void wait_counter(const uint32_t* counter,
+// Waits until *counter >= target (acquire) and returns true.  Bounded: after
+// `timeout_ns` it records kErrDepTimeout and returns false; it also returns
+// false at once when another block has already recorded an error, so one lost
+// signal cannot stall every block for the full timeout.
+__device__ __forceinline__ bool wait_counter(const uint32_t* counter,
                                              uint32_t target,
                                              uint64_t timeout_ns,
                                              unsigned* err) {
-  if (ld_acquire_u32(counter) >= target) return;
+  if (ld_acquire_u32(counter) >= target) return true;
   const uint64_t t0 = global_timer_ns();
   while (ld_acquire_u32(counter) < target) {
-    if (ld_volatile_u32(err) != 0u) return;
+    if (ld_volatile_u32(err) != 0u) return false;
     if (global_timer_ns() - t0 > timeout_ns) {
       atomicOr(err, kErrDepTimeout);
-      return;
+      return false;
     }
     __nanosleep(64);
   }
+  return true;
 }
 
 // ------------------------------------------------------ group-end table --
@@ -315,60 +386,58 @@ __device__ __forceinline__ void build_ends(const int32_t* __restrict__ offs,
   }
 }
 
-// First g in [0, n) with ends[g] > t (n if none).
-__device__ __forceinline__ int first_end_above(const int32_t* ends, int n,
-                                               int32_t t) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (ends[mid] > t)
-      hi = mid;
-    else
-      lo = mid + 1;
-  }
-  return lo;
-}
-
-// First g in [0, n) whose start (g ? ends[g-1] : 0) is >= t (n if none).
-// Starts are nondecreasing in g.
-__device__ __forceinline__ int first_start_at_or_above(const int32_t* ends,
-                                                       int n, int32_t t) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    const int32_t st = mid ? ends[mid - 1] : 0;
-    if (st >= t)
-      hi = mid;
-    else
-      lo = mid + 1;
-  }
-  return lo;
-}
-
-// Fills the segment part of a tile header for the token range [lo, hi).
+// The header of the tile with token range [lo, hi), built by one warp from
+// the group-end table: the nonempty group segments in the tile and the range
+// of groups whose scales the tile owns (the groups starting inside it; the
+// last tile of the token extent also owns those starting at or after its
+// start).  Groups are examined 32 at a time, from the block that holds the
+// first group ending at or after lo (found by probing the block ends).
 template <int kMaxSeg>
-__device__ __forceinline__ void fill_segments(TileHdr<kMaxSeg>& h,
-                                              const int32_t* ends, int n,
-                                              int32_t lo, int32_t hi,
-                                              bool last) {
-  h.lo = lo;
-  h.hi = hi;
-  h.last = last ? 1 : 0;
-  h.own_lo = first_start_at_or_above(ends, n, lo);
-  h.own_hi = last ? n : first_start_at_or_above(ends, n, hi);
-  int ns = 0;
-  for (int g = first_end_above(ends, n, lo); g < n; ++g) {
-    const int32_t s = g ? ends[g - 1] : 0;
-    if (s >= hi) break;
-    const int32_t a = max(s, lo), b = min(ends[g], hi);
-    if (b > a && ns < kMaxSeg) {
-      h.seg_g[ns] = g;
-      h.seg_lo[ns] = a - lo;
-      h.seg_hi[ns] = b - lo;
-      ++ns;
-    }
+__device__ __forceinline__ void build_header_warp(TileHdr<kMaxSeg>& h,
+                                                  const int32_t* ends, int n,
+                                                  int32_t lo, int32_t hi,
+                                                  bool last, int lane) {
+  int b0 = 0;
+  if (n > 32) {  // n <= 1024: one probe per block end
+    const int pe = 32 * lane + 31;
+    const unsigned m = __ballot_sync(0xffffffffu, pe >= n || ends[pe] >= lo);
+    b0 = m ? __ffs(m) - 1 : 32;  // 32: no group ends at or after lo
   }
-  h.nseg = ns;
+  const unsigned lt = (1u << lane) - 1u;
+  int ns = 0, own_lo = n, own_hi = 0;
+  for (int b = b0; 32 * b < n; ++b) {
+    const int g = 32 * b + lane;
+    const bool valid = g < n;
+    const int32_t s = valid ? (g ? ends[g - 1] : 0) : 0;
+    const int32_t e = valid ? ends[g] : 0;
+    const bool seg = valid && s < hi && e > lo && s < e;
+    const bool own = valid && s >= lo && (last || s < hi);
+    const unsigned ms = __ballot_sync(0xffffffffu, seg);
+    const unsigned mo = __ballot_sync(0xffffffffu, own);
+    if (seg) {
+      const int pos = ns + __popc(ms & lt);
+      if (pos < kMaxSeg) {
+        h.seg_g[pos] = static_cast<int16_t>(g);
+        h.seg_lo[pos] = static_cast<uint8_t>(max(s, lo) - lo);
+        h.seg_hi[pos] = static_cast<uint8_t>(min(e, hi) - lo);
+      }
+    }
+    ns += __popc(ms);
+    if (mo) {  // owned groups are contiguous
+      own_lo = min(own_lo, 32 * b + __ffs(mo) - 1);
+      own_hi = 32 * b + 32 - __clz(mo);
+    }
+    // starts are nondecreasing: once a start reaches hi, no later group has
+    // a segment here, and only the last tile owns groups starting later
+    if (!last && __ballot_sync(0xffffffffu, valid && s < hi) != 0xffffffffu) break;
+  }
+  if (lane == 0) {
+    h.lo = lo;
+    h.hi = hi;
+    h.nseg = min(ns, kMaxSeg);
+    h.own_lo = own_hi > 0 ? own_lo : 0;
+    h.own_hi = own_hi;
+  }
 }
 
 // ---------------------------------------------------------- ticket order --
@@ -378,39 +447,153 @@ struct Schedule {
   int32_t lag;     // 1 <= lag <= groups
 };
 
-struct Ticket {
-  int32_t phase;  // 0 = A, 1 = B
-  int32_t dg;     // dependency group
-  int32_t unit;   // tile within the group
-};
-
-// Order of blocks of `units` tickets:
+// Tickets come in blocks of `units` (one dependency group, one phase), in
+// the order
 //   A(0) .. A(L-1), then A(L), B(0), A(L+1), B(1), ..., A(G-1), B(G-1-L),
 //   then B(G-L) .. B(G-1).
-__device__ __forceinline__ Ticket decode_ticket(uint32_t t, const Schedule& s) {
-  Ticket k;
-  const int32_t b = static_cast<int32_t>(t / static_cast<uint32_t>(s.units));
-  k.unit = static_cast<int32_t>(t % static_cast<uint32_t>(s.units));
+// Block b holds tickets b * units .. b * units + units - 1; the unit is the
+// ticket's place in its block.  Returns the phase (0 = A, 1 = B) and group.
+__device__ __forceinline__ void decode_block(int32_t b, const Schedule& s,
+                                             int32_t& phase, int32_t& dg) {
   if (b < s.lag) {
-    k.phase = 0;
-    k.dg = b;
-    return k;
+    phase = 0;
+    dg = b;
+    return;
   }
   const int32_t i = b - s.lag;
   const int32_t pairs = s.groups - s.lag;
   if (i < 2 * pairs) {
-    if ((i & 1) == 0) {
-      k.phase = 0;
-      k.dg = s.lag + (i >> 1);
-    } else {
-      k.phase = 1;
-      k.dg = i >> 1;
-    }
+    phase = i & 1;
+    dg = (i & 1) ? (i >> 1) : s.lag + (i >> 1);
   } else {
-    k.phase = 1;
-    k.dg = pairs + (i - 2 * pairs);
+    phase = 1;
+    dg = pairs + (i - 2 * pairs);
   }
-  return k;
+}
+
+// Walks tickets first, first + stride, first + 2 stride, ... as (block,
+// unit) pairs without a division per step.
+struct TicketWalk {
+  int32_t block, unit;
+  int32_t q, r;  // stride = q * units + r
+  __device__ __forceinline__ TicketWalk(uint32_t first, uint32_t stride,
+                                        int32_t units) {
+    block = static_cast<int32_t>(first / static_cast<uint32_t>(units));
+    unit = static_cast<int32_t>(first % static_cast<uint32_t>(units));
+    q = static_cast<int32_t>(stride / static_cast<uint32_t>(units));
+    r = static_cast<int32_t>(stride % static_cast<uint32_t>(units));
+  }
+  __device__ __forceinline__ void next(int32_t units) {
+    block += q;
+    unit += r;
+    if (unit >= units) {
+      unit -= units;
+      ++block;
+    }
+  }
+};
+
+// Two fp32 products in one instruction, each rounded to nearest even like
+// __fmul_rn (no flush of subnormals).
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"((static_cast<uint64_t>(__float_as_uint(a.y)) << 32) | __float_as_uint(a.x)),
+        "l"((static_cast<uint64_t>(__float_as_uint(b.y)) << 32) | __float_as_uint(b.x)));
+  return make_float2(__uint_as_float(static_cast<uint32_t>(d)),
+                     __uint_as_float(static_cast<uint32_t>(d >> 32)));
+}
+
+// Eight bf16 (one 16-byte chunk) times eight scales -> eight e4m3 bytes
+// (lowest column in the lowest byte).
+__device__ __forceinline__ uint2 quant8(uint4 v, const float* sc) {
+  const float2 p0 = mul_f32x2(make_float2(bf16_lo(v.x), bf16_hi(v.x)), make_float2(sc[0], sc[1]));
+  const float2 p1 = mul_f32x2(make_float2(bf16_lo(v.y), bf16_hi(v.y)), make_float2(sc[2], sc[3]));
+  const float2 p2 = mul_f32x2(make_float2(bf16_lo(v.z), bf16_hi(v.z)), make_float2(sc[4], sc[5]));
+  const float2 p3 = mul_f32x2(make_float2(bf16_lo(v.w), bf16_hi(v.w)), make_float2(sc[6], sc[7]));
+  return make_uint2(cvt_e4m3x2(p0.x, p0.y) | (cvt_e4m3x2(p1.x, p1.y) << 16),
+                    cvt_e4m3x2(p2.x, p2.y) | (cvt_e4m3x2(p3.x, p3.y) << 16));
+}
+
+// ----------------------------------------------------------- signal ring --
+// Consumer warps -> signal lane: one slot per finished phase-A tile.  A
+// slot's full barrier counts one arrival per consumer warp (each after
+// __syncwarp, which orders that warp's amax atomics before it); its empty
+// barrier one arrival by the signal lane.
+template <int kSlots>
+struct SigRing {
+  uint64_t full[kSlots];
+  uint64_t empty[kSlots];
+  int32_t dg[kSlots];
+};
+
+constexpr int32_t kSigEnd = -1;   // the consumers are done
+constexpr int32_t kSigSkip = -2;  // a completion withheld (test hook)
+
+template <int kSlots>
+__device__ __forceinline__ void sig_init(SigRing<kSlots>& r, int consumer_warps) {
+  for (int i = 0; i < kSlots; ++i) {
+    mbar_init(&r.full[i], consumer_warps);
+    mbar_init(&r.empty[i], 1);
+  }
+}
+
+// Called by every consumer thread, in step (consumer warps never drift a
+// whole ring apart: they meet at a barrier on every tile).  Hands over a
+// finished phase-A tile of dependency group dg >= 0, kSigSkip or kSigEnd.
+template <int kSlots>
+__device__ __forceinline__ void sig_post(SigRing<kSlots>& r, int32_t dg, int t,
+                                         int lane, uint32_t& seq,
+                                         uint64_t timeout_ns, unsigned* err) {
+  const int slot = static_cast<int>(seq % kSlots);
+  const uint32_t par = (seq / kSlots) & 1u;
+  ++seq;
+  if (t == 0) {
+    mbar_wait(&r.empty[slot], par ^ 1u, timeout_ns, err);
+    r.dg[slot] = dg;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&r.full[slot]);
+}
+
+// The signal lane: takes the posted slots in order -- all that are already
+// posted each time it wakes -- and adds each run of equal groups to that
+// group's done counter with one release reduction.  Returns after kSigEnd
+// (or when a wait gives up).
+template <int kSlots>
+__device__ __forceinline__ void sig_loop(SigRing<kSlots>& r, uint32_t* done,
+                                         uint64_t timeout_ns, unsigned* err) {
+  uint32_t seq = 0;
+  for (;;) {
+    int slot = static_cast<int>(seq % kSlots);
+    uint32_t par = (seq / kSlots) & 1u;
+    if (!mbar_wait(&r.full[slot], par, timeout_ns, err)) return;
+    bool stop = false;
+    int32_t run_dg = -1;
+    uint32_t run = 0;
+    for (int n = 0;;) {
+      const int32_t dg = r.dg[slot];
+      mbar_arrive(&r.empty[slot]);
+      ++seq;
+      ++n;
+      if (dg == kSigEnd) stop = true;
+      if (dg >= 0) {
+        if (dg != run_dg) {
+          if (run) red_release_add(done + run_dg, run);
+          run_dg = dg;
+          run = 0;
+        }
+        ++run;
+      }
+      if (stop || n == kSlots) break;
+      slot = static_cast<int>(seq % kSlots);
+      par = (seq / kSlots) & 1u;
+      if (!mbar_test_wait(&r.full[slot], par)) break;
+    }
+    if (run) red_release_add(done + run_dg, run);
+    if (stop) return;
+  }
 }
 
 }  // namespace gq

@@ -24,7 +24,15 @@ struct DeviceInfo {
 struct DebugKnobs {
   int skip_arrival = 0;
   uint64_t timeout_ns = 1000000000ull;
+  int32_t lag[2] = {0, 0};  // per kind; 0 = automatic
 };
+
+// The lag of the ticket order: `forced` if positive, else enough dependency
+// groups that a producer running `stages` tiles ahead of its consumers on
+// each of `grid` CTAs stays clear of phase-B tiles whose group is unfinished;
+// clamped to [1, groups].
+int32_t schedule_lag(int32_t forced, int64_t units, int64_t groups,
+                     int64_t grid, int stages);
 
 // Encodes a 2-D tiled tensor map (row-major, dim0 innermost).
 gq_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype,
@@ -38,9 +46,9 @@ gq_status fail(gq_status st, const char* fmt, ...);
 // Returns GQ_ERR_CUDA with the runtime's message if `e` is an error.
 gq_status check_cuda(cudaError_t e, const char* what);
 
-// Workspace layout shared by both paths: a 256-byte counter header (ticket
-// counter first), then one done-counter per dependency group, then the amax
-// words.  Offsets in bytes.
+// Workspace layout shared by both paths: a 256-byte reserved header, then one
+// done-counter per dependency group, then the amax words.  Offsets in bytes;
+// every region starts on a 256-byte boundary.
 struct WorkspaceLayout {
   size_t counters = 0;  // start of the done counters
   size_t amax = 0;      // start of the amax words

@@ -188,6 +188,20 @@ int gq_version(void);
  */
 gq_status gq_debug_set(int skip_arrival, int64_t wait_timeout_ns);
 
+/*
+ * Tuning knob for the phase interleave of `kind` (GQ_KIND_COLWISE or
+ * GQ_KIND_ROWWISE_T).  Both kernels visit every tile twice -- phase A
+ * (amax) and phase B (scale + cast) -- and give phase A a lead of `lag`
+ * dependency groups (column slabs of 128 columns, or row bands of 128
+ * rows): phase A of group d + lag is scheduled before phase B of group d.
+ * A longer lead keeps phase B from waiting on unfinished amax words; a
+ * shorter one keeps the re-read tiles in L2.  lag = 0 restores the automatic
+ * choice; larger values are clamped to the number of groups.  Results do not
+ * depend on it.  Process-wide; not thread-safe with concurrent calls.
+ * Returns GQ_ERR_INVALID_ARG for an unknown kind or a negative lag.
+ */
+gq_status gq_set_lag(int kind, int32_t lag);
+
 #ifdef __cplusplus
 }
 #endif

@@ -181,6 +181,39 @@ def test_max_groups(gq):
     check_rowwise(gq, synth.Case("maxg_r", "rowwise_t", r.x, o, 0))
 
 
+@pytest.mark.parametrize("n_groups,tokens", [(65, 3000), (200, 6000), (1000, 20000)])
+def test_many_groups(gq, n_groups, tokens):
+    """More than 32 groups: the tile header is searched block by block over
+    the group-end table; tiles hold several segments, some more than the
+    stage carries amax words for, and group starts fall in every block."""
+    seed = 70 + n_groups
+    check_colwise(gq, synth.random_case("colwise", tokens, 144, n_groups, seed,
+                                        n_empty=n_groups // 10, align=1,
+                                        scale_mix=True, uncovered=5))
+    check_rowwise(gq, synth.random_case("rowwise_t", 144, tokens, n_groups,
+                                        seed + 1, n_empty=n_groups // 10,
+                                        align=1, scale_mix=True, uncovered=5))
+
+
+@pytest.mark.parametrize("lag", [1, 2, 5, 1000])
+def test_results_do_not_depend_on_lag(gq, lag):
+    """The phase interleave is a schedule choice: every lag, from the
+    shortest lead to all phase-A tiles before any phase-B tile, gives the
+    oracle's bytes."""
+    c = synth.random_case("colwise", 3000, 1040, 9, seed=80 + lag, n_empty=1,
+                          align=1, scale_mix=True, uncovered=3)
+    r = synth.random_case("rowwise_t", 1040, 3000, 9, seed=90 + lag, n_empty=1,
+                          align=1, scale_mix=True, uncovered=3)
+    try:
+        gq.set_lag(gq.GQ_KIND_COLWISE, lag)
+        gq.set_lag(gq.GQ_KIND_ROWWISE_T, lag)
+        check_colwise(gq, c)
+        check_rowwise(gq, r)
+    finally:
+        gq.set_lag(gq.GQ_KIND_COLWISE, 0)
+        gq.set_lag(gq.GQ_KIND_ROWWISE_T, 0)
+
+
 def test_element_map_exhaustive_amax(gq):
     """Every finite non-negative bf16 value as a column amax, each with 127
     elements of magnitude at most that amax (both signs, zeros, subnormals,

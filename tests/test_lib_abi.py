@@ -115,6 +115,15 @@ def test_debug_set_rejects_negative_timeout(gq):
     assert gq.lib().gq_debug_set(0, 0) == 0
 
 
+def test_set_lag_validation(gq):
+    lib = gq.lib()
+    assert lib.gq_set_lag(7, 1) == 1          # unknown kind
+    assert lib.gq_set_lag(0, -1) == 1         # negative lag
+    assert lib.gq_set_lag(0, 3) == 0
+    assert lib.gq_set_lag(1, 0) == 0
+    assert lib.gq_set_lag(0, 0) == 0          # back to automatic
+
+
 def test_binding_rejects_cpu_tensors(gq):
     import torch
     x = torch.zeros((16, 16), dtype=torch.bfloat16)
