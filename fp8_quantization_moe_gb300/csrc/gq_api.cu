@@ -140,12 +140,12 @@ gq_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype,
 }
 
 int32_t schedule_lag(int32_t forced, int64_t units, int64_t groups,
-                     int64_t grid, int stages) {
+                     int64_t grid, int lead) {
   // Phase B of group d starts 2 * lag * units tickets after the last phase-A
-  // ticket of d; the producers run up to stages * grid tickets ahead of the
+  // ticket of d; the producers run up to lead * grid tickets ahead of the
   // consumers, and CTAs drift apart by about grid more.
   int64_t lag = forced > 0 ? forced
-                           : ((stages + 2) * grid + 2 * units - 1) / (2 * units);
+                           : ((lead + 2) * grid + 2 * units - 1) / (2 * units);
   if (lag < 1) lag = 1;
   if (lag > groups) lag = groups;
   return static_cast<int32_t>(lag);

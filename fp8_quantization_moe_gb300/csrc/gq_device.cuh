@@ -4,33 +4,45 @@
 // schedule.
 //
 // Execution model (both kernels).  A persistent grid, launched cooperatively
-// so that every CTA is resident, of CTAs with two roles: a producer warp that
-// fills a ring of shared-memory stages, and consumer warps that process each
-// stage together.  A tile is visited twice: in phase A its |x| maxima are
-// folded into per-(group, column) or per-(row, group) amax words with
-// atomicMax; in phase B, once every phase-A tile its amax words depend on is
-// done, it is re-read, scaled and cast.  Tiles that share amax words form a
-// "dependency group" (a column slab for colwise, a row band for rowwise_t).
-// Tickets follow a fixed order in which phase A of dependency group d+L
-// precedes phase B of group d (L = the lag), so that by the time phase B of a
-// group comes up its phase-A tiles are long finished and its bytes still sit
-// in L2 (loaded with evict_last): HBM sees one read of the input.  CTA c
-// takes tickets c, c + grid, c + 2 grid, ... in that order.
+// so that every CTA is resident, of CTAs with three roles: a producer warp
+// that fills a ring of 16 KB shared-memory stages by TMA, eight consumer
+// warps that each work on every stage independently, and a signal lane.
 //
-// For every ticket the producer warp builds the tile header (the group
-// segments inside the tile), starts the TMA load of the tile and, in phase
-// B, first waits for the dependency group to be complete and then copies the
-// amax words of the tile's first segments into the stage with cp.async, so
-// that the consumers neither wait on other CTAs nor on L2 latency for them.
-// Finished phase-A tiles leave the consumers through a small ring of
-// shared-memory slots to a signal lane, which publishes them on the groups'
-// done counters with release reductions: the memory fence that publishing
-// implies stalls that lane only, never the consumers.
+// Work comes in super tiles of kSub stages (4 x 64 = 256 consecutive tokens
+// of one column slab or row band).  Each super tile is visited twice: in
+// phase A its |x| maxima are folded into per-(group, column) or per-(row,
+// group) amax words with atomicMax; in phase B, once every phase-A super
+// tile its amax words depend on is done, it is re-read, scaled and cast.
+// Tiles that share amax words form a "dependency group" (a column slab for
+// colwise, a row band for rowwise_t).  Tickets follow a fixed order in which
+// phase A of dependency group d+L precedes phase B of group d (L = the lag),
+// so that by the time phase B of a group comes up its phase-A tiles are long
+// finished and its bytes still sit in L2 (loaded with evict_last): HBM sees
+// one read of the input.  CTA c takes tickets c, c + grid, c + 2 grid, ...
+// in that order.
+//
+// Per ticket the producer writes a context -- the super tile's header (its
+// group segments) and, in phase B, the amax words of its first segments,
+// copied with cp.async -- and loads the kSub stages.  Consumer warps carry
+// per-segment state (maxima, scales) across the stages of a super tile, so
+// the per-segment work -- reductions, atomics, divisions -- is paid once per
+// 256 tokens.
+//
+// The signal lane runs an event loop with two jobs.  (1) Finished phase-A
+// super tiles reach it through a small ring of shared-memory slots; it
+// publishes them on the groups' done counters with release reductions, so
+// the memory fence that publishing implies never stalls a consumer.  (2) It
+// walks the CTA's own ticket sequence ahead of the producer and, for each
+// dependency group a phase-B ticket will need, polls the group's done counter
+// (acquire) and then raises a shared-memory flag (release); the producer
+// waits on the flag, so the global round trips of dependency checks leave
+// its critical path.
 //
 // Progress: all CTAs are resident and each takes its tickets in increasing
 // order, so the smallest unfinished ticket can always advance -- its phase-A
-// dependencies have smaller tickets -- and the schedule cannot deadlock.
-// Every wait is nonetheless bounded in time.
+// dependencies have smaller tickets -- and the schedule cannot deadlock; the
+// signal lane never blocks on a dependency while completions wait in its
+// ring.  Every wait is nonetheless bounded in time.
 #pragma once
 
 #include <cuda.h>
@@ -49,20 +61,20 @@ constexpr unsigned kErrDepTimeout = 1u;   // a dependency-group wait expired
 constexpr unsigned kErrMbarTimeout = 2u;  // an mbarrier wait expired
 
 // ------------------------------------------------------------ tile header --
-// Written by the producer warp into shared memory next to each stage; read by
-// the consumers after the stage's full barrier completes.  Segment bounds are
-// relative to lo and at most 255 (tiles span at most 128 tokens).
+// Header of a super tile, written by the producer warp into a context and
+// read by the consumers once the super tile's first stage is full.  Segment
+// bounds are relative to lo.
 template <int kMaxSeg>
 struct alignas(16) TileHdr {
   int32_t phase;   // 0 = A (amax), 1 = B (scale + cast), -1 = stop
   int32_t dg;      // dependency group
-  int32_t lo, hi;  // token range [lo, hi) of the tile, clamped to the extent
+  int32_t lo, hi;  // token range [lo, hi) of the super tile, clamped to the extent
   int32_t own_lo, own_hi;  // groups whose scales phase B of this tile writes
   int32_t nseg;            // nonempty group segments inside [lo, hi)
-  int32_t unit;            // tile within the dependency group
+  int32_t nsub;            // stages (64-token sub-tiles) of the super tile
   int16_t seg_g[kMaxSeg];
-  uint8_t seg_lo[kMaxSeg];
-  uint8_t seg_hi[kMaxSeg];
+  uint16_t seg_lo[kMaxSeg];
+  uint16_t seg_hi[kMaxSeg];
 };
 
 // ---------------------------------------------------------- PTX wrappers --
@@ -344,25 +356,18 @@ __device__ __forceinline__ uint32_t ld_volatile_u32(const unsigned* p) {
   return *reinterpret_cast<const volatile unsigned*>(p);
 }
 
-// Waits until *counter >= target (acquire) and returns true.  Bounded: after
-// `timeout_ns` it records kErrDepTimeout and returns false; it also returns
-// false at once when another block has already recorded an error, so one lost
-// signal cannot stall every block for the full timeout.
-__device__ __forceinline__ bool wait_counter(const uint32_t* counter,
-                                             uint32_t target,
-                                             uint64_t timeout_ns,
-                                             unsigned* err) {
-  if (ld_acquire_u32(counter) >= target) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (ld_acquire_u32(counter) < target) {
-    if (ld_volatile_u32(err) != 0u) return false;
-    if (global_timer_ns() - t0 > timeout_ns) {
-      atomicOr(err, kErrDepTimeout);
-      return false;
-    }
-    __nanosleep(64);
-  }
-  return true;
+__device__ __forceinline__ void st_release_cta_s32(int32_t* p, int32_t v) {
+  asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v)
+               : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_acquire_cta_s32(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];"
+               : "=r"(v)
+               : "r"(smem_addr(p))
+               : "memory");
+  return v;
 }
 
 // ------------------------------------------------------ group-end table --
@@ -418,8 +423,8 @@ __device__ __forceinline__ void build_header_warp(TileHdr<kMaxSeg>& h,
       const int pos = ns + __popc(ms & lt);
       if (pos < kMaxSeg) {
         h.seg_g[pos] = static_cast<int16_t>(g);
-        h.seg_lo[pos] = static_cast<uint8_t>(max(s, lo) - lo);
-        h.seg_hi[pos] = static_cast<uint8_t>(min(e, hi) - lo);
+        h.seg_lo[pos] = static_cast<uint16_t>(max(s, lo) - lo);
+        h.seg_hi[pos] = static_cast<uint16_t>(min(e, hi) - lo);
       }
     }
     ns += __popc(ms);
@@ -557,27 +562,61 @@ __device__ __forceinline__ void sig_post(SigRing<kSlots>& r, int32_t dg, int t,
   if (lane == 0) mbar_arrive(&r.full[slot]);
 }
 
-// The signal lane: takes the posted slots in order -- all that are already
-// posted each time it wakes -- and adds each run of equal groups to that
-// group's done counter with one release reduction.  Returns after kSigEnd
-// (or when a wait gives up).
+// Dependency readiness, written by the signal lane, read by the producer.
+struct DepFlag {
+  int32_t ready;  // every dependency group <= ready that this CTA needs is complete
+  int32_t fail;   // 1 once the signal lane gave up waiting
+};
+
+// The next dependency group > last that a phase-B ticket of the walk needs
+// (-1 when the walk is exhausted); the walk advances past that ticket.
+__device__ __forceinline__ int32_t next_b_group(TicketWalk& tw, const Schedule& s,
+                                                int32_t last) {
+  const int32_t blocks = 2 * s.groups;
+  for (; tw.block < blocks; tw.next(s.units)) {
+    int32_t phase, dg;
+    decode_block(tw.block, s, phase, dg);
+    if (phase == 1 && dg > last) {
+      tw.next(s.units);
+      return dg;
+    }
+  }
+  return -1;
+}
+
+// The signal lane's event loop.  (1) Takes the posted slots in order -- all
+// that are posted each time round -- and adds each run of equal groups to
+// that group's done counter with one release reduction.  (2) Walks the
+// CTA's tickets ahead of the producer: for the next dependency group a
+// phase-B ticket needs, probes its done counter (acquire) once per round and,
+// when it has reached `target`, publishes the group in f.ready (release).
+// It never blocks on a dependency, so this CTA's own completions keep
+// flowing.  Returns after kSigEnd.  Gives up a dependency after timeout_ns
+// (kErrDepTimeout, f.fail = 1) and the ring after idle_ns without any event.
 template <int kSlots>
-__device__ __forceinline__ void sig_loop(SigRing<kSlots>& r, uint32_t* done,
-                                         uint64_t timeout_ns, unsigned* err) {
+__device__ __forceinline__ void signal_lane(SigRing<kSlots>& r, DepFlag& f,
+                                            uint32_t* done, const Schedule& sched,
+                                            uint32_t target, uint64_t timeout_ns,
+                                            uint64_t idle_ns, unsigned* err) {
+  TicketWalk tw(blockIdx.x, gridDim.x, sched.units);
+  int32_t want = next_b_group(tw, sched, -1);
   uint32_t seq = 0;
+  uint64_t t_event = global_timer_ns(), t_want = t_event;
   for (;;) {
-    int slot = static_cast<int>(seq % kSlots);
-    uint32_t par = (seq / kSlots) & 1u;
-    if (!mbar_wait(&r.full[slot], par, timeout_ns, err)) return;
-    bool stop = false;
+    bool progress = false, stop = false;
     int32_t run_dg = -1;
     uint32_t run = 0;
-    for (int n = 0;;) {
+    for (int n = 0; n < kSlots; ++n) {
+      const int slot = static_cast<int>(seq % kSlots);
+      if (!mbar_test_wait(&r.full[slot], (seq / kSlots) & 1u)) break;
       const int32_t dg = r.dg[slot];
       mbar_arrive(&r.empty[slot]);
       ++seq;
-      ++n;
-      if (dg == kSigEnd) stop = true;
+      progress = true;
+      if (dg == kSigEnd) {
+        stop = true;
+        break;
+      }
       if (dg >= 0) {
         if (dg != run_dg) {
           if (run) red_release_add(done + run_dg, run);
@@ -586,13 +625,49 @@ __device__ __forceinline__ void sig_loop(SigRing<kSlots>& r, uint32_t* done,
         }
         ++run;
       }
-      if (stop || n == kSlots) break;
-      slot = static_cast<int>(seq % kSlots);
-      par = (seq / kSlots) & 1u;
-      if (!mbar_test_wait(&r.full[slot], par)) break;
     }
     if (run) red_release_add(done + run_dg, run);
     if (stop) return;
+    const uint64_t now = global_timer_ns();
+    if (want >= 0) {
+      if (ld_acquire_u32(done + want) >= target) {
+        st_release_cta_s32(&f.ready, want);
+        want = next_b_group(tw, sched, want);
+        t_want = now;
+        progress = true;
+      } else if (ld_volatile_u32(err) != 0u || now - t_want > timeout_ns) {
+        if (ld_volatile_u32(err) == 0u) atomicOr(err, kErrDepTimeout);
+        st_release_cta_s32(&f.fail, 1);
+        want = -1;
+      }
+    }
+    if (progress) {
+      t_event = now;
+    } else {
+      if (now - t_event > idle_ns) {
+        atomicOr(err, kErrMbarTimeout);
+        st_release_cta_s32(&f.fail, 1);
+        return;
+      }
+      __nanosleep(want >= 0 ? 64 : 256);
+    }
+  }
+}
+
+// Producer side: waits until f.ready >= dg.  False when the signal lane gave
+// up, an error is recorded elsewhere, or timeout_ns passes.
+__device__ __forceinline__ bool wait_dep_flag(DepFlag& f, int32_t dg,
+                                              uint64_t timeout_ns, unsigned* err) {
+  if (ld_acquire_cta_s32(&f.ready) >= dg) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (ld_acquire_cta_s32(&f.ready) >= dg) return true;
+    if (ld_acquire_cta_s32(&f.fail) != 0) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      atomicOr(err, kErrDepTimeout);
+      return false;
+    }
+    __nanosleep(32);
   }
 }
 

@@ -28,11 +28,11 @@ struct DebugKnobs {
 };
 
 // The lag of the ticket order: `forced` if positive, else enough dependency
-// groups that a producer running `stages` tiles ahead of its consumers on
-// each of `grid` CTAs stays clear of phase-B tiles whose group is unfinished;
-// clamped to [1, groups].
+// groups that a producer running `lead` tickets ahead of its consumers on
+// each of `grid` CTAs stays clear of phase-B tickets whose group is
+// unfinished; clamped to [1, groups].
 int32_t schedule_lag(int32_t forced, int64_t units, int64_t groups,
-                     int64_t grid, int stages);
+                     int64_t grid, int lead);
 
 // Encodes a 2-D tiled tensor map (row-major, dim0 innermost).
 gq_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype,
