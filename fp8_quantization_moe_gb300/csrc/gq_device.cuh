@@ -4,45 +4,54 @@
 // schedule.
 //
 // Execution model (both kernels).  A persistent grid, launched cooperatively
-// so that every CTA is resident, of CTAs with three roles: a producer warp
-// that fills a ring of 16 KB shared-memory stages by TMA, eight consumer
-// warps that each work on every stage independently, and a signal lane.
+// so that every CTA is resident, of CTAs with four roles: a context warp, a
+// producer warp, consumer warps and a signal lane.
 //
-// Work comes in super tiles of kSub stages (4 x 64 = 256 consecutive tokens
-// of one column slab or row band).  Each super tile is visited twice: in
-// phase A its |x| maxima are folded into per-(group, column) or per-(row,
-// group) amax words with atomicMax; in phase B, once every phase-A super
-// tile its amax words depend on is done, it is re-read, scaled and cast.
-// Tiles that share amax words form a "dependency group" (a column slab for
-// colwise, a row band for rowwise_t).  Tickets follow a fixed order in which
-// phase A of dependency group d+L precedes phase B of group d (L = the lag),
-// so that by the time phase B of a group comes up its phase-A tiles are long
-// finished and its bytes still sit in L2 (loaded with evict_last): HBM sees
-// one read of the input.  CTA c takes tickets c, c + grid, c + 2 grid, ...
-// in that order.
+// Work comes in tickets: super tiles of kSub stages (256 consecutive tokens
+// of one column slab or row band; a stage is 8 KB).  Each super tile is
+// visited twice: in phase A the |x| maxima of its stages are folded into
+// per-(group, column) or per-(row, group) amax words with atomicMax; in
+// phase B, once every phase-A super tile its amax words depend on is done,
+// it is re-read, scaled and cast.  Tiles that share amax words form a
+// "dependency group" (a column slab for colwise, a row band for rowwise_t).
+// Tickets are numbered in an order in which phase A of dependency group d+L
+// precedes phase B of group d (L = the lag), so that by the time phase B of
+// a group comes up its phase-A tiles are finished and its bytes still sit in
+// L2 (loaded with evict_last): HBM sees one read of the input.  CTAs claim
+// tickets from a global counter, so tickets are taken roughly in that order
+// whatever the pace of each CTA.
 //
-// Per ticket the producer writes a context -- the super tile's header (its
-// group segments) and, in phase B, the amax words of its first segments,
-// copied with cp.async -- and loads the kSub stages.  Consumer warps carry
-// per-segment state (maxima, scales) across the stages of a super tile, so
-// the per-segment work -- reductions, atomics, divisions -- is paid once per
-// 256 tokens.
+// The context warp claims the CTA's tickets, one ahead, and writes a context
+// per ticket into a small ring: first the ticket itself (published at once,
+// so that the producer can start loading), then -- in phase B after the
+// dependency group is complete -- the super tile's header (its group
+// segments) and the amax words of its first segments, copied with cp.async.
+// The producer warp follows the published tickets and loads their stages,
+// in order, into a shared ring of stage buffers with TMA, tagging each with
+// its ticket and place.  A consumer warp takes the next loaded stage (a
+// shared counter), whichever ticket it belongs to, and does all the work of
+// that stage alone, with no barrier among warps, so the per-stage
+// bookkeeping (the waits, the segment walk, the scale divisions) is paid
+// once per 8 KB.  In phase A the warps fold their stage maxima into the
+// context with shared-memory atomics; the warp that finishes a super tile's
+// last stage (an acquire-release counter in the context tells it) adds them
+// to the global amax words, one atomicMax per (segment, column or row), and
+// posts the super tile to the signal lane.
 //
 // The signal lane runs an event loop with two jobs.  (1) Finished phase-A
 // super tiles reach it through a small ring of shared-memory slots; it
 // publishes them on the groups' done counters with release reductions, so
-// the memory fence that publishing implies never stalls a consumer.  (2) It
-// walks the CTA's own ticket sequence ahead of the producer and, for each
-// dependency group a phase-B ticket will need, polls the group's done counter
-// (acquire) and then raises a shared-memory flag (release); the producer
-// waits on the flag, so the global round trips of dependency checks leave
-// its critical path.
+// the memory fence that publishing implies never stalls a consumer.  (2)
+// When the context warp waits for a dependency group, it polls the group's
+// done counter (acquire) and then raises a shared-memory flag (release).
 //
-// Progress: all CTAs are resident and each takes its tickets in increasing
-// order, so the smallest unfinished ticket can always advance -- its phase-A
-// dependencies have smaller tickets -- and the schedule cannot deadlock; the
-// signal lane never blocks on a dependency while completions wait in its
-// ring.  Every wait is nonetheless bounded in time.
+// Progress: all CTAs are resident and each processes its tickets in
+// increasing order, so the smallest unfinished ticket can always advance --
+// its phase-A dependencies have smaller tickets, claimed by running CTAs;
+// within a CTA, stages are loaded and claimed in ticket order, so the stages
+// of a ticket never wait behind those of a later one -- and the schedule
+// cannot deadlock; the signal lane never blocks on a dependency while
+// completions wait in its ring.  Every wait is nonetheless bounded in time.
 #pragma once
 
 #include <cuda.h>
@@ -61,17 +70,17 @@ constexpr unsigned kErrDepTimeout = 1u;   // a dependency-group wait expired
 constexpr unsigned kErrMbarTimeout = 2u;  // an mbarrier wait expired
 
 // ------------------------------------------------------------ tile header --
-// Header of a super tile, written by the producer warp into a context and
-// read by the consumers once the super tile's first stage is full.  Segment
+// Header of a super tile, written by the context warp into a context and
+// read by the consumers once the context is full.  Segment
 // bounds are relative to lo.
 template <int kMaxSeg>
 struct alignas(16) TileHdr {
-  int32_t phase;   // 0 = A (amax), 1 = B (scale + cast), -1 = stop
+  int32_t phase;   // 0 = A (amax), 1 = B (scale + cast)
   int32_t dg;      // dependency group
   int32_t lo, hi;  // token range [lo, hi) of the super tile, clamped to the extent
   int32_t own_lo, own_hi;  // groups whose scales phase B of this tile writes
   int32_t nseg;            // nonempty group segments inside [lo, hi)
-  int32_t nsub;            // stages (64-token sub-tiles) of the super tile
+  int32_t nsub;            // stages of the super tile (a short last tile has fewer)
   int16_t seg_g[kMaxSeg];
   uint16_t seg_lo[kMaxSeg];
   uint16_t seg_hi[kMaxSeg];
@@ -253,45 +262,53 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Named barrier among `nthreads` threads (id 0 is __syncthreads).
-__device__ __forceinline__ void named_bar(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Named barrier that also ORs a predicate over the participating threads, so
-// that they all take the same branch afterwards.
-__device__ __forceinline__ bool named_bar_any(int id, int nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
+// Returns v unchanged, but the compiler must assume it changed here: the
+// addresses of the pure shared loads below are derived from a value pinned
+// after the stage's full barrier, so those loads cannot be issued before the
+// wait.  (They cannot sink past the stage's release either: their values
+// feed stores and atomics that precede it.)
+__device__ __forceinline__ uint32_t pin(uint32_t v) {
+  asm volatile("" : "+r"(v)::"memory");
   return v;
 }
 
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+// Shared-memory atomic max (u32) and acquire-release add at CTA scope.
+__device__ __forceinline__ void red_max_shared(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta_shared(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// 16-byte shared load; pure, so the compiler may overlap it with other work.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "r"(addr));
+  return v;
 }
 
 // ldmatrix x4 transposed: four 8x8 b16 matrices; lane l supplies the row
 // address of row (l & 7) of matrix (l >> 3).  Lane l receives, for matrix j,
 // the b16 pair at stored rows 2*(l&3) and 2*(l&3)+1 of column (l >> 2).
+// Pure, like lds128.
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0,
                                               uint32_t& r1, uint32_t& r2,
                                               uint32_t& r3) {
-  asm volatile(
+  asm(
       "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
       : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
       : "r"(addr));
@@ -311,21 +328,6 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t amax_bits_of(uint32_t acc) {
   const uint32_t lo = acc & 0x7FFFu, hi = (acc >> 16) & 0x7FFFu;
   return (lo > hi ? lo : hi) << 16;
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) {
-  return __uint_as_float(w << 16);
-}
-__device__ __forceinline__ float bf16_hi(uint32_t w) {
-  return __uint_as_float(w & 0xFFFF0000u);
-}
-
-// Two fp32 -> packed e4m3x2, round-to-nearest-even, saturating to +-448
-// (`lo` lands in the low byte).
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return static_cast<uint32_t>(r);
 }
 
 // scale = 448 / max(amax, 1e-12), IEEE fp32 round-to-nearest division.
@@ -498,109 +500,120 @@ struct TicketWalk {
   }
 };
 
-// Two fp32 products in one instruction, each rounded to nearest even like
-// __fmul_rn (no flush of subnormals).
-__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;"
-      : "=l"(d)
-      : "l"((static_cast<uint64_t>(__float_as_uint(a.y)) << 32) | __float_as_uint(a.x)),
-        "l"((static_cast<uint64_t>(__float_as_uint(b.y)) << 32) | __float_as_uint(b.x)));
-  return make_float2(__uint_as_float(static_cast<uint32_t>(d)),
-                     __uint_as_float(static_cast<uint32_t>(d >> 32)));
+// Four e4m3 bytes from two bf16x2 words w0 = (x0, x1), w1 = (x2, x3) and
+// four scales: byte i = e4m3(fp32(x_i * s_i)), x0 in the lowest byte.  The
+// products are IEEE fp32 multiplies rounded to nearest even (mul.rn.f32x2,
+// no flush of subnormals); the cast rounds to nearest even and saturates to
+// +-448 (cvt.rn.satfinite).  A bf16 value is the upper half of its fp32.
+__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, float s0,
+                                          float s1, float s2, float s3) {
+  uint32_t out;
+  asm("{\n\t"
+      ".reg .b32 a0, a1, a2, a3;\n\t"
+      ".reg .b64 x0, x1, k0, k1, y0, y1;\n\t"
+      ".reg .b16 h0, h1;\n\t"
+      "shl.b32 a0, %1, 16;\n\t"
+      "and.b32 a1, %1, 0xFFFF0000;\n\t"
+      "shl.b32 a2, %2, 16;\n\t"
+      "and.b32 a3, %2, 0xFFFF0000;\n\t"
+      "mov.b64 x0, {a0, a1};\n\t"
+      "mov.b64 x1, {a2, a3};\n\t"
+      "mov.b64 k0, {%3, %4};\n\t"
+      "mov.b64 k1, {%5, %6};\n\t"
+      "mul.rn.f32x2 y0, x0, k0;\n\t"
+      "mul.rn.f32x2 y1, x1, k1;\n\t"
+      "mov.b64 {a0, a1}, y0;\n\t"
+      "mov.b64 {a2, a3}, y1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h0, a1, a0;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h1, a3, a2;\n\t"
+      "mov.b32 %0, {h0, h1};\n\t"
+      "}"
+      : "=r"(out)
+      : "r"(w0), "r"(w1), "f"(s0), "f"(s1), "f"(s2), "f"(s3));
+  return out;
 }
 
 // Eight bf16 (one 16-byte chunk) times eight scales -> eight e4m3 bytes
 // (lowest column in the lowest byte).
 __device__ __forceinline__ uint2 quant8(uint4 v, const float* sc) {
-  const float2 p0 = mul_f32x2(make_float2(bf16_lo(v.x), bf16_hi(v.x)), make_float2(sc[0], sc[1]));
-  const float2 p1 = mul_f32x2(make_float2(bf16_lo(v.y), bf16_hi(v.y)), make_float2(sc[2], sc[3]));
-  const float2 p2 = mul_f32x2(make_float2(bf16_lo(v.z), bf16_hi(v.z)), make_float2(sc[4], sc[5]));
-  const float2 p3 = mul_f32x2(make_float2(bf16_lo(v.w), bf16_hi(v.w)), make_float2(sc[6], sc[7]));
-  return make_uint2(cvt_e4m3x2(p0.x, p0.y) | (cvt_e4m3x2(p1.x, p1.y) << 16),
-                    cvt_e4m3x2(p2.x, p2.y) | (cvt_e4m3x2(p3.x, p3.y) << 16));
+  return make_uint2(quant4(v.x, v.y, sc[0], sc[1], sc[2], sc[3]),
+                    quant4(v.z, v.w, sc[4], sc[5], sc[6], sc[7]));
 }
 
 // ----------------------------------------------------------- signal ring --
-// Consumer warps -> signal lane: one slot per finished phase-A tile.  A
-// slot's full barrier counts one arrival per consumer warp (each after
-// __syncwarp, which orders that warp's amax atomics before it); its empty
-// barrier one arrival by the signal lane.
+// Consumer warps -> signal lane: one slot per finished phase-A super tile, taken
+// in the order of a shared claim counter.  A slot's full barrier counts the
+// posting warp's lane-0 arrival (after __syncwarp, which orders the warp's
+// amax atomics before it); its empty barrier the signal lane's.  Only the
+// warp that flushes a super tile's maxima posts it.
 template <int kSlots>
 struct SigRing {
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
   int32_t dg[kSlots];
+  uint32_t head;  // next slot sequence number to claim
 };
 
-constexpr int32_t kSigEnd = -1;   // the consumers are done
+constexpr int32_t kSigEnd = -1;   // a consumer warp is done
 constexpr int32_t kSigSkip = -2;  // a completion withheld (test hook)
 
 template <int kSlots>
-__device__ __forceinline__ void sig_init(SigRing<kSlots>& r, int consumer_warps) {
+__device__ __forceinline__ void sig_init(SigRing<kSlots>& r) {
   for (int i = 0; i < kSlots; ++i) {
-    mbar_init(&r.full[i], consumer_warps);
+    mbar_init(&r.full[i], 1);
     mbar_init(&r.empty[i], 1);
   }
+  r.head = 0;
 }
 
-// Called by every consumer thread, in step (consumer warps never drift a
-// whole ring apart: they meet at a barrier on every tile).  Hands over a
-// finished phase-A tile of dependency group dg >= 0, kSigSkip or kSigEnd.
+// Called by a whole consumer warp: hands over a finished phase-A super tile of
+// dependency group dg >= 0, kSigSkip or kSigEnd.  At most one post per warp
+// is outstanding and there are fewer warps than slots, so a claimed slot's
+// previous round is the one its empty barrier last completed.
 template <int kSlots>
-__device__ __forceinline__ void sig_post(SigRing<kSlots>& r, int32_t dg, int t,
-                                         int lane, uint32_t& seq,
+__device__ __forceinline__ void sig_post(SigRing<kSlots>& r, int32_t dg, int lane,
                                          uint64_t timeout_ns, unsigned* err) {
-  const int slot = static_cast<int>(seq % kSlots);
-  const uint32_t par = (seq / kSlots) & 1u;
-  ++seq;
-  if (t == 0) {
-    mbar_wait(&r.empty[slot], par ^ 1u, timeout_ns, err);
+  __syncwarp();
+  if (lane == 0) {
+    const uint32_t seq = atomicAdd(&r.head, 1u);
+    const int slot = static_cast<int>(seq % kSlots);
+    mbar_wait(&r.empty[slot], ((seq / kSlots) & 1u) ^ 1u, timeout_ns, err);
     r.dg[slot] = dg;
+    mbar_arrive(&r.full[slot]);
   }
   __syncwarp();
-  if (lane == 0) mbar_arrive(&r.full[slot]);
 }
 
-// Dependency readiness, written by the signal lane, read by the producer.
+// Dependency readiness, shared by the context warp and the signal lane.
 struct DepFlag {
-  int32_t ready;  // every dependency group <= ready that this CTA needs is complete
+  int32_t want;   // dependency group the context warp waits for (-1: none)
+  int32_t ready;  // largest dependency group seen complete (-1: none)
   int32_t fail;   // 1 once the signal lane gave up waiting
 };
 
-// The next dependency group > last that a phase-B ticket of the walk needs
-// (-1 when the walk is exhausted); the walk advances past that ticket.
-__device__ __forceinline__ int32_t next_b_group(TicketWalk& tw, const Schedule& s,
-                                                int32_t last) {
-  const int32_t blocks = 2 * s.groups;
-  for (; tw.block < blocks; tw.next(s.units)) {
-    int32_t phase, dg;
-    decode_block(tw.block, s, phase, dg);
-    if (phase == 1 && dg > last) {
-      tw.next(s.units);
-      return dg;
-    }
-  }
-  return -1;
+__device__ __forceinline__ void dep_init(DepFlag& f) {
+  f.want = -1;
+  f.ready = -1;
+  f.fail = 0;
 }
 
 // The signal lane's event loop.  (1) Takes the posted slots in order -- all
 // that are posted each time round -- and adds each run of equal groups to
-// that group's done counter with one release reduction.  (2) Walks the
-// CTA's tickets ahead of the producer: for the next dependency group a
-// phase-B ticket needs, probes its done counter (acquire) once per round and,
-// when it has reached `target`, publishes the group in f.ready (release).
-// It never blocks on a dependency, so this CTA's own completions keep
-// flowing.  Returns after kSigEnd.  Gives up a dependency after timeout_ns
+// that group's done counter with one release reduction.  (2) When the
+// context warp waits for a dependency group (f.want), probes the group's done
+// counter (acquire) once per round and, when it has reached `target`,
+// publishes the group in f.ready (release).  It never blocks on a
+// dependency, so this CTA's own completions keep flowing.  Returns after
+// `posters` kSigEnd posts.  Gives up a dependency after timeout_ns
 // (kErrDepTimeout, f.fail = 1) and the ring after idle_ns without any event.
 template <int kSlots>
 __device__ __forceinline__ void signal_lane(SigRing<kSlots>& r, DepFlag& f,
-                                            uint32_t* done, const Schedule& sched,
-                                            uint32_t target, uint64_t timeout_ns,
-                                            uint64_t idle_ns, unsigned* err) {
-  TicketWalk tw(blockIdx.x, gridDim.x, sched.units);
-  int32_t want = next_b_group(tw, sched, -1);
+                                            uint32_t* done, uint32_t target, int posters,
+                                            uint64_t timeout_ns, uint64_t idle_ns,
+                                            unsigned* err) {
   uint32_t seq = 0;
+  int ended = 0;
+  int32_t ready = -1, watched = -1;
   uint64_t t_event = global_timer_ns(), t_want = t_event;
   for (;;) {
     bool progress = false, stop = false;
@@ -614,8 +627,11 @@ __device__ __forceinline__ void signal_lane(SigRing<kSlots>& r, DepFlag& f,
       ++seq;
       progress = true;
       if (dg == kSigEnd) {
-        stop = true;
-        break;
+        if (++ended == posters) {
+          stop = true;
+          break;
+        }
+        continue;
       }
       if (dg >= 0) {
         if (dg != run_dg) {
@@ -629,16 +645,19 @@ __device__ __forceinline__ void signal_lane(SigRing<kSlots>& r, DepFlag& f,
     if (run) red_release_add(done + run_dg, run);
     if (stop) return;
     const uint64_t now = global_timer_ns();
-    if (want >= 0) {
+    const int32_t want = *reinterpret_cast<volatile int32_t*>(&f.want);
+    if (want != watched) {
+      watched = want;
+      t_want = now;
+    }
+    if (want > ready) {
       if (ld_acquire_u32(done + want) >= target) {
+        ready = want;
         st_release_cta_s32(&f.ready, want);
-        want = next_b_group(tw, sched, want);
-        t_want = now;
         progress = true;
       } else if (ld_volatile_u32(err) != 0u || now - t_want > timeout_ns) {
         if (ld_volatile_u32(err) == 0u) atomicOr(err, kErrDepTimeout);
         st_release_cta_s32(&f.fail, 1);
-        want = -1;
       }
     }
     if (progress) {
@@ -649,16 +668,18 @@ __device__ __forceinline__ void signal_lane(SigRing<kSlots>& r, DepFlag& f,
         st_release_cta_s32(&f.fail, 1);
         return;
       }
-      __nanosleep(want >= 0 ? 64 : 256);
+      __nanosleep(want > ready ? 64 : 256);
     }
   }
 }
 
-// Producer side: waits until f.ready >= dg.  False when the signal lane gave
-// up, an error is recorded elsewhere, or timeout_ns passes.
+// Context-warp side: announces dependency group dg and waits until it is
+// complete.  False when the signal lane gave up, an error is recorded
+// elsewhere, or timeout_ns passes.
 __device__ __forceinline__ bool wait_dep_flag(DepFlag& f, int32_t dg,
                                               uint64_t timeout_ns, unsigned* err) {
   if (ld_acquire_cta_s32(&f.ready) >= dg) return true;
+  *reinterpret_cast<volatile int32_t*>(&f.want) = dg;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (ld_acquire_cta_s32(&f.ready) >= dg) return true;
@@ -669,6 +690,12 @@ __device__ __forceinline__ bool wait_dep_flag(DepFlag& f, int32_t dg,
     }
     __nanosleep(32);
   }
+}
+
+// Tickets are claimed from a global counter, in increasing order; ticket t
+// is unit t % units of block t / units.
+__device__ __forceinline__ uint32_t claim_ticket(uint32_t* counter) {
+  return atomicAdd(counter, 1u);
 }
 
 }  // namespace gq

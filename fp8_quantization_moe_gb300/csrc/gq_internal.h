@@ -57,8 +57,7 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int64_t dep_groups, int64_t amax_words);
 
 namespace colwise {
-constexpr int kW = 128;  // columns per slab
-constexpr int kR = 64;   // token rows per tile
+constexpr int kW = 128;  // columns per slab (dependency group)
 gq_status setup(DeviceInfo& info);
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
                  int32_t M, int32_t K, const int32_t* offs, int32_t G,
@@ -66,8 +65,8 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
 }  // namespace colwise
 
 namespace rowwise {
-constexpr int kTn = 128;  // rows of A per tile (bytes per output row run)
-constexpr int kTm = 64;   // token columns per tile
+constexpr int kTn = 64;  // rows of A per stage: one row band (dependency group)
+constexpr int kTm = 64;  // token columns per stage
 gq_status setup(DeviceInfo& info);
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
                  int32_t N, int32_t Mg, const int32_t* offs, int32_t G,

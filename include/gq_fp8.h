@@ -79,7 +79,8 @@ typedef enum gq_status {
  *   kind GQ_KIND_COLWISE:   rows = M, cols = K.
  *   kind GQ_KIND_ROWWISE_T: rows = N, cols = Mg.
  * The workspace holds the per-(group, column) or per-(row, group) running
- * amax words and the work-claiming counters; the call clears it itself, so
+ * amax words and one completion counter per column slab (128 columns) or
+ * row band (64 rows); the call clears it itself, so
  * its contents on entry do not matter.  Returns 0 when no workspace is
  * needed (empty problems) and for invalid arguments.
  */

@@ -214,6 +214,17 @@ def test_results_do_not_depend_on_lag(gq, lag):
         gq.set_lag(gq.GQ_KIND_ROWWISE_T, 0)
 
 
+def test_short_super_tiles_many_tickets(gq):
+    """Token extents that end in a short super tile (fewer stages than
+    consumer warps), with several super tiles per CTA: warps that have no
+    stage in a super tile must still read its ticket before releasing its
+    context.  320 tokens = one full super tile of 256 + one of 64."""
+    check_colwise(gq, synth.random_case("colwise", 320, 65536, 5, seed=81,
+                                        n_empty=1, align=1, scale_mix=True))
+    check_rowwise(gq, synth.random_case("rowwise_t", 65536, 320, 5, seed=82,
+                                        n_empty=1, align=1, scale_mix=True))
+
+
 def test_element_map_exhaustive_amax(gq):
     """Every finite non-negative bf16 value as a column amax, each with 127
     elements of magnitude at most that amax (both signs, zeros, subnormals,
