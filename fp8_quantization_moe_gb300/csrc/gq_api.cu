@@ -232,9 +232,7 @@ size_t gq_workspace_bytes(int kind, int64_t rows, int64_t cols,
   if (kind == GQ_KIND_ROWWISE_T) {
     const int64_t N = rows, Mg = cols;
     if (N == 0 || Mg == 0) return 0;
-    return workspace_layout((N + rowwise::kTn - 1) / rowwise::kTn,
-                            N * static_cast<int64_t>(n_groups))
-        .total;
+    return rowwise::kWorkspaceBytes;
   }
   return 0;
 }

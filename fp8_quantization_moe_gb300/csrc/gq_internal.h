@@ -46,9 +46,9 @@ gq_status fail(gq_status st, const char* fmt, ...);
 // Returns GQ_ERR_CUDA with the runtime's message if `e` is an error.
 gq_status check_cuda(cudaError_t e, const char* what);
 
-// Workspace layout shared by both paths: a 256-byte reserved header, then one
-// done-counter per dependency group, then the amax words.  Offsets in bytes;
-// every region starts on a 256-byte boundary.
+// Colwise workspace layout: a 256-byte header (the ticket counter first),
+// then one done-counter per dependency group, then the amax words.  Offsets
+// in bytes; every region starts on a 256-byte boundary.
 struct WorkspaceLayout {
   size_t counters = 0;  // start of the done counters
   size_t amax = 0;      // start of the amax words
@@ -65,8 +65,9 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
 }  // namespace colwise
 
 namespace rowwise {
-constexpr int kTn = 64;  // rows of A per stage: one row band (dependency group)
-constexpr int kTm = 64;  // token columns per stage
+constexpr int kTn = 64;  // rows of A per window: one row band
+constexpr int kTm = 64;  // token columns per window
+constexpr size_t kWorkspaceBytes = 256;  // the unit counter, padded
 gq_status setup(DeviceInfo& info);
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
                  int32_t N, int32_t Mg, const int32_t* offs, int32_t G,

@@ -78,10 +78,11 @@ typedef enum gq_status {
  * Workspace size in bytes for one call.
  *   kind GQ_KIND_COLWISE:   rows = M, cols = K.
  *   kind GQ_KIND_ROWWISE_T: rows = N, cols = Mg.
- * The workspace holds the per-(group, column) or per-(row, group) running
- * amax words and one completion counter per column slab (128 columns) or
- * row band (64 rows); the call clears it itself, so
- * its contents on entry do not matter.  Returns 0 when no workspace is
+ * Colwise: a work counter, one completion counter per column slab (128
+ * columns) and the per-(group, column) running amax words.  Rowwise_t: a
+ * work counter only (256 bytes), since each (row band, group) pair is
+ * finished by one thread block.  The call clears what it uses itself, so
+ * the contents on entry do not matter.  Returns 0 when no workspace is
  * needed (empty problems) and for invalid arguments.
  */
 size_t gq_workspace_bytes(int kind, int64_t rows, int64_t cols,
@@ -180,26 +181,28 @@ const char* gq_last_error(void);
 int gq_version(void);
 
 /*
- * Test hook for the bounded cross-block waits.  wait_timeout_ns sets the
- * limit after which a waiting kernel gives up (0 restores the 1 s default).
- * skip_arrival != 0 makes the next launches omit one thread block's
- * completion signal -- the first phase-A tile of the first column slab (or
- * row band) -- so that its waiters must time out and report
+ * Test hook for the bounded waits.  wait_timeout_ns sets the limit after
+ * which a waiting kernel gives up (0 restores the 1 s default).
+ * skip_arrival != 0 makes the next launches omit one completion signal --
+ * colwise: the first phase-A tile of the first column slab, whose waiters
+ * are other thread blocks; rowwise_t: the amax-complete signal of the
+ * (first row band, first group) unit, whose waiters are the warps that
+ * would cast it -- so that the waiters must time out and report
  * GQ_ERR_TIMEOUT.  Process-wide; not thread-safe with concurrent calls.
  */
 gq_status gq_debug_set(int skip_arrival, int64_t wait_timeout_ns);
 
 /*
- * Tuning knob for the phase interleave of `kind` (GQ_KIND_COLWISE or
- * GQ_KIND_ROWWISE_T).  Both kernels visit every tile twice -- phase A
- * (amax) and phase B (scale + cast) -- and give phase A a lead of `lag`
- * dependency groups (column slabs of 128 columns, or row bands of 128
- * rows): phase A of group d + lag is scheduled before phase B of group d.
- * A longer lead keeps phase B from waiting on unfinished amax words; a
- * shorter one keeps the re-read tiles in L2.  lag = 0 restores the automatic
- * choice; larger values are clamped to the number of groups.  Results do not
- * depend on it.  Process-wide; not thread-safe with concurrent calls.
- * Returns GQ_ERR_INVALID_ARG for an unknown kind or a negative lag.
+ * Tuning knob for the phase interleave of `kind`.  The colwise kernel
+ * visits every tile twice -- phase A (amax) and phase B (scale + cast) --
+ * and gives phase A a lead of `lag` column slabs (128 columns each): phase
+ * A of slab d + lag is scheduled before phase B of slab d.  A longer lead
+ * keeps phase B from waiting on unfinished amax words; a shorter one keeps
+ * the re-read tiles in L2.  lag = 0 restores the automatic choice; larger
+ * values are clamped to the number of slabs.  Results do not depend on it.
+ * GQ_KIND_ROWWISE_T is accepted and has no effect: that kernel has no
+ * cross-block schedule.  Process-wide; not thread-safe with concurrent
+ * calls.  Returns GQ_ERR_INVALID_ARG for an unknown kind or a negative lag.
  */
 gq_status gq_set_lag(int kind, int32_t lag);
 

@@ -214,6 +214,27 @@ def test_results_do_not_depend_on_lag(gq, lag):
         gq.set_lag(gq.GQ_KIND_ROWWISE_T, 0)
 
 
+@pytest.mark.parametrize("widths,lead", [
+    ((768, 760, 776, 768), 0),        # 12, 12, 13 (straddles), 12 windows
+    ((764, 772, 8, 1540, 64), 4),     # starts off the 8-token grid
+    ((5000, 3, 1, 1100), 1),          # long groups and one-token groups
+    ((800, 700, 900, 640, 1000), 0),  # long and resident units alternate
+])
+def test_rowwise_resident_and_long_units(gq, widths, lead):
+    """Groups around the number of windows a unit may keep in shared memory
+    between its two passes (12 windows of 64 tokens): units just inside,
+    just past (a group whose first window starts below it, rounded down to 8
+    tokens) and far past it, which stream twice; plus groups of one token."""
+    widths = list(widths)
+    Mg = lead + sum(widths)
+    Mg += (-Mg) % 8
+    offs = np.cumsum([lead + widths[0]] + widths[1:]).astype(np.int32)
+    base = synth.random_case("rowwise_t", 80, Mg, 1, seed=300 + len(widths),
+                             align=8, scale_mix=True)
+    check_rowwise(gq, synth.Case("resident_" + "_".join(map(str, widths)),
+                                 "rowwise_t", base.x, offs, 0))
+
+
 def test_short_super_tiles_many_tickets(gq):
     """Token extents that end in a short super tile (fewer stages than
     consumer warps), with several super tiles per CTA: warps that have no
