@@ -24,9 +24,9 @@
 // longer unit streams its windows twice through the ring, the second time
 // from L2 where it can.
 //
-// One producer thread claims units, publishes each in a small ring of unit
+// A producer warp claims units, publishes each in a small ring of unit
 // descriptors, and issues the TMA loads of the block's window stream into a
-// ring of kStages windows.  Pass A of a unit folds its amax, pass B scales,
+// ring of kStages windows, kIssue windows side by side.  Pass A of a unit folds its amax, pass B scales,
 // casts and stores it; a pass covers the unit's windows in order.  Resident
 // units are visited with a lag of one unit,
 //   A(r0), A(r1), B(r0), A(r2), B(r1), ...,
@@ -40,12 +40,12 @@
 //   A visit: lane l takes rows l and l + 32 of the window, folds |x| over
 //     the window's columns inside the group with max.xorsign.abs.bf16x2 and
 //     adds the row maxima to the unit's amax words with shared-memory
-//     atomics; after its A visits of a unit, every warp arrives on the
-//     unit's amax barrier;
-//   B visit: once that barrier completes (a warp with no B visit in the unit
-//     goes on to the next unit), the warp turns the amax words into
-//     scales (448 / max(amax, 1e-12), IEEE division) and, for each 32-row
-//     half and 8-column chunk, ldmatrix.x4.trans gives lane l the pairs
+//     atomics; the last warp through a unit's pass A (an acquire-release
+//     counter says which) turns its amax words into scales (448 / max(amax,
+//     1e-12), IEEE division), stores them, and completes the unit's amax
+//     barrier;
+//   B visit: once that barrier completes, for each 32-row half and 8-column
+//     chunk, ldmatrix.x4.trans gives lane l the pairs
 //     (n, n+1) of rows 8i + 2(l%4) of column 8c + l/4, which are multiplied
 //     in fp32 (mul.rn.f32x2) and packed with cvt.rn.satfinite.e4m3x2; a 4x4
 //     exchange of byte pairs among the four lanes of a column leaves each
@@ -71,12 +71,14 @@ constexpr int kFit = 12;     // windows a unit may keep resident between passes
 constexpr int kUnits = 4;    // unit descriptors in flight
 constexpr int kConsumerWarps = 8;
 constexpr int kAhead = 2;  // units a block claims before it needs them
+constexpr int kIssue = 8;  // producer lanes issuing window loads side by side
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kQ = kTn / 32;  // 32-row halves of a window
 constexpr int kStageBytes = kTn * kTm * 2;
 static_assert(kTm * 2 == 128 && kTn == 64, "128-byte swizzled rows, two 32-row halves");
 static_assert(2 * kFit <= kStages, "the ring holds two consecutive resident units");
+static_assert(kIssue <= kStages && kIssue <= 32, "a batch of loads takes distinct slots");
 
 struct Unit {
   int32_t n0;   // first row of the band; -1: no more units
@@ -86,8 +88,10 @@ struct Unit {
   int32_t hi;
   int32_t nst;  // windows
   int32_t resident;  // 1: windows stay in the ring for pass B
-  int32_t hold;      // test hook: warp 0 never reports the amax complete
+  int32_t hold;      // test hook: the amax is never reported complete
+  uint32_t a_done;   // consumer warps through with pass A
   alignas(16) uint32_t amax[kTn];  // row maxima, fp32 bit patterns
+  alignas(16) float scale[kTn];    // written by the last warp through pass A
 };
 
 struct Smem {
@@ -96,7 +100,7 @@ struct Smem {
   uint64_t full[kStages];    // window loaded (TMA bytes)
   uint64_t empty[kStages];   // window released
   uint64_t u_full[kUnits];   // descriptor published
-  uint64_t u_amax[kUnits];   // every warp's A visits done (W arrivals)
+  uint64_t u_amax[kUnits];   // pass A done and scales written
   uint64_t u_free[kUnits];   // every warp's B visits done (W arrivals)
   int32_t ends[kMaxGroups];
 };
@@ -115,42 +119,52 @@ struct Params {
   int32_t skip_arrival;
 };
 
-// ------------------------------------------------------- producer thread --
-// Loads the window at (x, y) into the next slot of the ring.
-__device__ __forceinline__ bool load_window(Smem& s, const CUtensorMap* amap, uint32_t& g,
-                                            int32_t x, int32_t y, uint64_t pol,
-                                            uint64_t wait_ns, unsigned* err) {
-  const int st = static_cast<int>(g % kStages);
-  if (!mbar_wait(&s.empty[st], ((g / kStages) & 1) ^ 1u, wait_ns, err)) return false;
-  mbar_arrive_expect_tx(&s.full[st], kStageBytes);
-  tma_load_2d(s.tile[st], amap, x, y, &s.full[st], pol);
-  ++g;
+// --------------------------------------------------------- producer warp --
+// Loads the nst windows of a pass (token columns x0 + 64 k, rows y ...) into
+// the ring: lanes 0 .. kIssue-1 take windows kb + lane side by side, each
+// waiting for its own slot.
+__device__ __forceinline__ bool load_pass(Smem& s, const CUtensorMap* amap, uint32_t& g, int nst,
+                                          int32_t x0, int32_t y, uint64_t pol, int lane,
+                                          uint64_t wait_ns, unsigned* err) {
+  for (int kb = 0; kb < nst; kb += kIssue) {
+    const int k = kb + lane;
+    bool ok = true;
+    if (lane < kIssue && k < nst) {
+      const uint32_t ld = g + k;
+      const int st = static_cast<int>(ld % kStages);
+      ok = mbar_wait(&s.empty[st], ((ld / kStages) & 1) ^ 1u, wait_ns, err);
+      if (ok) {
+        mbar_arrive_expect_tx(&s.full[st], kStageBytes);
+        tma_load_2d(s.tile[st], amap, x0 + k * kTm, y, &s.full[st], pol);
+      }
+    }
+    if (__any_sync(0xffffffffu, !ok)) return false;
+  }
+  g += static_cast<uint32_t>(nst);
   return true;
 }
 
-// The whole warp builds the group-end table; one thread runs the rest.
 __device__ __forceinline__ void producer_warp(Smem& s, const CUtensorMap* amap,
                                               const Params& p, int lane) {
   build_ends(p.offs, p.G, p.Mg, s.ends, lane);
   __syncwarp();
-  if (lane != 0) return;
-  prefetch_tensormap(amap);
+  if (lane == 0) prefetch_tensormap(amap);
   const uint64_t pol_once = policy_evict_first();  // read once
   const uint64_t pol_again = policy_evict_last();  // a long unit's pass A
   const uint64_t wait_ns = 4 * p.timeout_ns;
   uint32_t g = 0;     // loads issued
   uint32_t useq = 0;  // units published
   bool ok = true;
-  // units are claimed kAhead ahead, so that a claim's round trip to L2
+  // lane 0 claims units kAhead ahead, so that a claim's round trip to L2
   // overlaps the loads of the units before it
   uint32_t q[kAhead];
 #pragma unroll
-  for (int a = 0; a < kAhead; ++a) q[a] = claim_ticket(p.ticket);
+  for (int a = 0; a < kAhead; ++a) q[a] = lane == 0 ? claim_ticket(p.ticket) : 0u;
   for (;;) {
-    const uint32_t u = q[0];
+    const uint32_t u = __shfl_sync(0xffffffffu, q[0], 0);
 #pragma unroll
     for (int a = 0; a + 1 < kAhead; ++a) q[a] = q[a + 1];
-    if (u < p.units) q[kAhead - 1] = claim_ticket(p.ticket);
+    if (lane == 0 && u < p.units) q[kAhead - 1] = claim_ticket(p.ticket);
     int32_t grp = 0, n0 = -1, s0 = 0, e0 = 0;
     if (u < p.units) {  // else: publish the stop descriptor
       grp = static_cast<int32_t>(u % static_cast<uint32_t>(p.G));
@@ -159,8 +173,11 @@ __device__ __forceinline__ void producer_warp(Smem& s, const CUtensorMap* amap,
       e0 = s.ends[grp];
       if (e0 == s0) {  // empty group: amax 0 for every row
         const float e = scale_from_amax_bits(0u);
-        for (int r = 0; r < kTn && n0 + r < p.N; ++r)
-          p.scales[static_cast<size_t>(n0 + r) * p.G + grp] = e;
+#pragma unroll
+        for (int qq = 0; qq < kQ; ++qq) {
+          const int32_t n = n0 + lane + 32 * qq;
+          if (n < p.N) p.scales[static_cast<size_t>(n) * p.G + grp] = e;
+        }
         continue;
       }
     }
@@ -169,31 +186,32 @@ __device__ __forceinline__ void producer_warp(Smem& s, const CUtensorMap* amap,
     const bool resident = nst <= kFit;
     const int us = static_cast<int>(useq % kUnits);
     ok = mbar_wait(&s.u_free[us], ((useq / kUnits) & 1) ^ 1u, wait_ns, p.err);
-    if (!ok) break;
+    if (__any_sync(0xffffffffu, !ok)) break;
     Unit& U = s.unit[us];
-#pragma unroll
-    for (int r = 0; r < kTn; r += 4) sts128(smem_addr(&U.amax[r]), make_uint4(0, 0, 0, 0));
-    U.n0 = n0;
-    U.g = grp;
-    U.x0 = x0;
-    U.lo = s0 - x0;
-    U.hi = e0 - x0;
-    U.nst = nst;
-    U.resident = resident ? 1 : 0;
-    U.hold = p.skip_arrival && u == 0u;
-    mbar_arrive(&s.u_full[us]);
+    if (lane < kTn / 4) sts128(smem_addr(&U.amax[4 * lane]), make_uint4(0, 0, 0, 0));
+    if (lane == 0) {
+      U.n0 = n0;
+      U.g = grp;
+      U.x0 = x0;
+      U.lo = s0 - x0;
+      U.hi = e0 - x0;
+      U.nst = nst;
+      U.resident = resident ? 1 : 0;
+      U.hold = p.skip_arrival && u == 0u;
+      U.a_done = 0u;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.u_full[us]);
     ++useq;
     // the stream's loads: pass A of the unit; a long unit's pass B at once
-    for (int k = 0; k < nst && ok; ++k)
-      ok = load_window(s, amap, g, x0 + k * kTm, n0, resident ? pol_once : pol_again, wait_ns,
-                       p.err);
-    for (int k = 0; !resident && k < nst && ok; ++k)
-      ok = load_window(s, amap, g, x0 + k * kTm, n0, pol_once, wait_ns, p.err);
+    ok = load_pass(s, amap, g, nst, x0, n0, resident ? pol_once : pol_again, lane, wait_ns, p.err);
+    if (ok && !resident) ok = load_pass(s, amap, g, nst, x0, n0, pol_once, lane, wait_ns, p.err);
     if (!ok || n0 < 0) break;
   }
   // no load may still be in flight when the block exits
-  for (uint32_t d = g > static_cast<uint32_t>(kStages) ? g - kStages : 0u; d < g; ++d)
-    mbar_wait(&s.full[d % kStages], (d / kStages) & 1, wait_ns, p.err);
+  if (lane == 0)
+    for (uint32_t d = g > static_cast<uint32_t>(kStages) ? g - kStages : 0u; d < g; ++d)
+      mbar_wait(&s.full[d % kStages], (d / kStages) & 1, wait_ns, p.err);
 }
 
 // ------------------------------------------------------------ consumers --
@@ -251,10 +269,14 @@ __device__ __forceinline__ void fold_a(Unit& U, int ca, int cb, uint32_t tile, i
 }
 
 // B visit: scale, cast and transpose the window at token column xw (group
-// columns [ca, cb) of it); store rows of A^T.  sq[qq] is the scale of row
-// n0 + lane + 32 qq.
+// columns [ca, cb) of it); store rows of A^T.  scale[r] is the scale of row
+// n0 + r.  Each 32-row half goes through the steps in batches of
+// all eight 8-column chunks -- loads, casts, the two exchanges, stores -- so
+// that eight independent chains hide the latency of each step; chunks
+// outside [ca, cb) are computed from the window's other columns and not
+// stored.
 __device__ __forceinline__ void quant_b(int32_t n0, int32_t xw, int ca, int cb,
-                                        const float (&sq)[kQ], uint32_t tile, const Params& p,
+                                        const float* scale, uint32_t tile, const Params& p,
                                         int lane) {
   const int q = lane & 3;
   const int mcol = lane >> 2;  // column within an 8-column chunk
@@ -262,34 +284,48 @@ __device__ __forceinline__ void quant_b(int32_t n0, int32_t xw, int ca, int cb,
   uint8_t* obase = p.out_t + static_cast<size_t>(xw + mcol) * p.N + n0 + 8 * q;
   const size_t N8 = 8 * static_cast<size_t>(p.N);
   const uint32_t lrow = tile + static_cast<uint32_t>(lane) * 128u;  // ldmatrix row address base
-  const int c_first = max(ca, 0) >> 3;
-  const int c_last = (min(cb, kTm) - 1) >> 3;
+  constexpr int kC = kTm / 8;  // chunks
 #pragma unroll
   for (int qq = 0; qq < kQ; ++qq) {
     // scales of rows 32 qq + 8 i + 2q (+1), the rows of matrix i
     float sv[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      sv[2 * i] = __shfl_sync(0xffffffffu, sq[qq], 8 * i + 2 * q);
-      sv[2 * i + 1] = __shfl_sync(0xffffffffu, sq[qq], 8 * i + 2 * q + 1);
+      const float2 v = *reinterpret_cast<const float2*>(scale + 32 * qq + 8 * i + 2 * q);
+      sv[2 * i] = v.x;
+      sv[2 * i + 1] = v.y;
+    }
+    uint32_t r[kC][4];
+#pragma unroll
+    for (int cc = 0; cc < kC; ++cc)
+      ldsm_x4_trans(lrow + qq * 32 * 128 + ((((cc ^ lane) & 7)) << 4), r[cc][0], r[cc][1],
+                    r[cc][2], r[cc][3]);
+    // p01: bytes of rows 2q, 2q+1 (matrix 0) and 8+2q, 9+2q (matrix 1);
+    // p23: matrices 2 and 3 -- the pairs V[q][i] of lane q
+    uint32_t p01[kC], p23[kC];
+#pragma unroll
+    for (int cc = 0; cc < kC; ++cc) {
+      p01[cc] = quant4(r[cc][0], r[cc][1], sv[0], sv[1], sv[2], sv[3]);
+      p23[cc] = quant4(r[cc][2], r[cc][3], sv[4], sv[5], sv[6], sv[7]);
+    }
+    // 4x4 transpose of pairs among the lanes of one column: lane q ends
+    // with V[0][q], V[1][q], V[2][q], V[3][q] = rows 8q .. 8q + 7
+    uint32_t tlo[kC], thi[kC];
+#pragma unroll
+    for (int cc = 0; cc < kC; ++cc) {
+      const uint32_t x1 = __shfl_xor_sync(0xffffffffu, (q & 2) ? p01[cc] : p23[cc], 2);
+      tlo[cc] = (q & 2) ? x1 : p01[cc];
+      thi[cc] = (q & 2) ? p23[cc] : x1;
     }
     const bool st_ok = n0 + 32 * qq + 8 * q < p.N;
-#pragma unroll 2
-    for (int cc = c_first; cc <= c_last; ++cc) {
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4_trans(lrow + qq * 32 * 128 + ((((cc ^ lane) & 7)) << 4), r0, r1, r2, r3);
-      // p01: bytes of rows 2q, 2q+1 (matrix 0) and 8+2q, 9+2q (matrix 1);
-      // p23: matrices 2 and 3 -- the pairs V[q][i] of lane q
-      const uint32_t p01 = quant4(r0, r1, sv[0], sv[1], sv[2], sv[3]);
-      const uint32_t p23 = quant4(r2, r3, sv[4], sv[5], sv[6], sv[7]);
-      // 4x4 transpose of pairs among the lanes of one column: lane q ends
-      // with V[0][q], V[1][q], V[2][q], V[3][q] = rows 8q .. 8q + 7
-      const uint32_t x1 = __shfl_xor_sync(0xffffffffu, (q & 2) ? p01 : p23, 2);
-      const uint32_t tlo = (q & 2) ? x1 : p01, thi = (q & 2) ? p23 : x1;
+#pragma unroll
+    for (int cc = 0; cc < kC; ++cc) {
       const uint32_t x2 = __shfl_xor_sync(
-          0xffffffffu, __byte_perm(tlo, thi, (q & 1) ? 0x5410 : 0x7632), 1);
-      const uint32_t w0 = (q & 1) ? __byte_perm(x2, tlo, 0x7610) : __byte_perm(tlo, x2, 0x5410);
-      const uint32_t w1 = (q & 1) ? __byte_perm(x2, thi, 0x7632) : __byte_perm(thi, x2, 0x7610);
+          0xffffffffu, __byte_perm(tlo[cc], thi[cc], (q & 1) ? 0x5410 : 0x7632), 1);
+      const uint32_t w0 =
+          (q & 1) ? __byte_perm(x2, tlo[cc], 0x7610) : __byte_perm(tlo[cc], x2, 0x5410);
+      const uint32_t w1 =
+          (q & 1) ? __byte_perm(x2, thi[cc], 0x7632) : __byte_perm(thi[cc], x2, 0x7610);
       const int m = cc * 8 + mcol;  // window column
       if (m >= ca && m < cb && st_ok)
         __stcs(reinterpret_cast<uint2*>(obase + cc * N8 + qq * 32), make_uint2(w0, w1));
@@ -318,7 +354,8 @@ __device__ __forceinline__ bool wait_load(Smem& s, uint32_t ld, uint64_t wait_ns
 // Pass A of unit `cu` (its windows are ring loads cu.first ...): this warp's
 // visits, then its arrival on the unit's amax barrier.
 __device__ __forceinline__ bool pass_a(Smem& s, const UnitView& cu, bool hold, uint32_t& j,
-                                       int w, int lane, uint64_t wait_ns, unsigned* err) {
+                                       const Params& p, int w, int lane, uint64_t wait_ns) {
+  unsigned* err = p.err;
   Unit& U = s.unit[cu.useq % kUnits];
   for (int k = static_cast<int>((w + kConsumerWarps - j % kConsumerWarps) % kConsumerWarps);
        k < cu.nst; k += kConsumerWarps) {
@@ -333,32 +370,35 @@ __device__ __forceinline__ bool pass_a(Smem& s, const UnitView& cu, bool hold, u
     }
   }
   j += static_cast<uint32_t>(cu.nst);
+  // the last warp through pass A (an acquire-release counter says which)
+  // turns the amax words into the unit's scales, once
   __syncwarp();
-  if (lane == 0 && !(hold && w == 0)) mbar_arrive(&s.u_amax[cu.useq % kUnits]);
+  uint32_t prev = 0;
+  if (lane == 0) prev = atom_add_acq_rel_cta_shared(smem_addr(&U.a_done), 1u);
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+  if (prev + 1 == static_cast<uint32_t>(kConsumerWarps)) {
+#pragma unroll
+    for (int qq = 0; qq < kQ; ++qq) {
+      const int r = lane + 32 * qq;
+      const float sc = scale_from_amax_bits(U.amax[r]);
+      U.scale[r] = sc;
+      if (cu.n0 + r < p.N) p.scales[static_cast<size_t>(cu.n0 + r) * p.G + cu.g] = sc;
+    }
+    __syncwarp();
+    if (lane == 0 && !hold) mbar_arrive(&s.u_amax[cu.useq % kUnits]);
+  }
   return true;
 }
 
 // Pass B of unit `pv`, whose windows are ring loads `base` ...: this warp's
-// visits (and, for one warp per unit, the scale stores), then its arrival on
-// the unit's free barrier.
+// visits, then its arrival on the unit's free barrier.
 __device__ __forceinline__ bool pass_b(Smem& s, const UnitView& pv, uint32_t base, uint32_t& j,
                                        const Params& p, int w, int lane, uint64_t wait_ns) {
   const int ps = static_cast<int>(pv.useq % kUnits);
   const int k0 = static_cast<int>((w + kConsumerWarps - j % kConsumerWarps) % kConsumerWarps);
-  const bool writer = pv.useq % kConsumerWarps == static_cast<uint32_t>(w);
-  if (k0 < pv.nst || writer) {
+  if (k0 < pv.nst) {
     bool ok = mbar_wait(&s.u_amax[ps], (pv.useq / kUnits) & 1, wait_ns, p.err);
     if (__any_sync(0xffffffffu, !ok)) return false;
-    float sq[kQ];
-#pragma unroll
-    for (int qq = 0; qq < kQ; ++qq) sq[qq] = scale_from_amax_bits(s.unit[ps].amax[lane + 32 * qq]);
-    if (writer) {
-#pragma unroll
-      for (int qq = 0; qq < kQ; ++qq) {
-        const int32_t n = pv.n0 + lane + 32 * qq;
-        if (n < p.N) p.scales[static_cast<size_t>(n) * p.G + pv.g] = sq[qq];
-      }
-    }
     for (int k = k0; k < pv.nst; k += kConsumerWarps) {
       const uint32_t ld = base + k;
       // a resident window is still in the round its A visit waited for
@@ -366,7 +406,8 @@ __device__ __forceinline__ bool pass_b(Smem& s, const UnitView& pv, uint32_t bas
                        : wait_load(s, ld, wait_ns, p.err);
       if (__any_sync(0xffffffffu, !ok)) return false;
       const uint32_t tile = pin(smem_addr(s.tile[ld % kStages]));
-      quant_b(pv.n0, pv.x0 + k * kTm, pv.lo - k * kTm, pv.hi - k * kTm, sq, tile, p, lane);
+      quant_b(pv.n0, pv.x0 + k * kTm, pv.lo - k * kTm, pv.hi - k * kTm, s.unit[ps].scale, tile, p,
+              lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.empty[ld % kStages]);
     }
@@ -405,7 +446,7 @@ __device__ __forceinline__ void consumer_warp(Smem& s, const Params& p, int w, i
     }
     if (cu.resident) {
       g += static_cast<uint32_t>(cu.nst);
-      if (!pass_a(s, cu, hold, j, w, lane, wait_ns, p.err)) return;
+      if (!pass_a(s, cu, hold, j, p, w, lane, wait_ns)) return;
       if (pending && !pass_b(s, pv, pv.first, j, p, w, lane, wait_ns)) return;
       pv = cu;
       pending = true;
@@ -413,7 +454,7 @@ __device__ __forceinline__ void consumer_warp(Smem& s, const Params& p, int w, i
       if (pending && !pass_b(s, pv, pv.first, j, p, w, lane, wait_ns)) return;
       pending = false;
       g += static_cast<uint32_t>(cu.nst);
-      if (!pass_a(s, cu, hold, j, w, lane, wait_ns, p.err)) return;
+      if (!pass_a(s, cu, hold, j, p, w, lane, wait_ns)) return;
       const uint32_t base = g;  // the windows come again
       g += static_cast<uint32_t>(cu.nst);
       if (!pass_b(s, cu, base, j, p, w, lane, wait_ns)) return;
@@ -436,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kUnits; ++i) {
       mbar_init(&s.u_full[i], 1);
-      mbar_init(&s.u_amax[i], kConsumerWarps);
+      mbar_init(&s.u_amax[i], 1);
       mbar_init(&s.u_free[i], kConsumerWarps);
     }
     fence_mbar_init();
