@@ -151,12 +151,12 @@ int32_t schedule_lag(int32_t forced, int64_t units, int64_t groups,
   return static_cast<int32_t>(lag);
 }
 
-WorkspaceLayout workspace_layout(int64_t dep_groups, int64_t amax_words) {
+WorkspaceLayout colwise_workspace(int64_t K, int64_t G) {
   auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
   WorkspaceLayout L;
   L.counters = 256;
-  L.amax = L.counters + up(static_cast<size_t>(dep_groups) * 4);
-  L.total = L.amax + up(static_cast<size_t>(amax_words) * 4);
+  L.amax = L.counters + up(static_cast<size_t>((K + 63) / 64) * 4);
+  L.total = L.amax + up(static_cast<size_t>(G * K) * 4);
   return L;
 }
 
@@ -225,9 +225,7 @@ size_t gq_workspace_bytes(int kind, int64_t rows, int64_t cols,
   if (kind == GQ_KIND_COLWISE) {
     const int64_t M = rows, K = cols;
     if (M == 0 || K == 0) return 0;
-    return workspace_layout((K + colwise::kW - 1) / colwise::kW,
-                            static_cast<int64_t>(n_groups) * K)
-        .total;
+    return colwise_workspace(K, n_groups).total;
   }
   if (kind == GQ_KIND_ROWWISE_T) {
     const int64_t N = rows, Mg = cols;

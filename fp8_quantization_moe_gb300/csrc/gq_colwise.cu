@@ -522,8 +522,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   p.sched.lag = schedule_lag(dbg.lag[GQ_KIND_COLWISE], p.sched.units, p.sched.groups,
                              grid, kCtx);
 
-  const WorkspaceLayout L =
-      workspace_layout(p.sched.groups, static_cast<int64_t>(G) * K);
+  const WorkspaceLayout L = colwise_workspace(K, G);
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.offs = offs;
   p.ticket = reinterpret_cast<uint32_t*>(w);  // first word of the header

@@ -47,14 +47,15 @@ gq_status fail(gq_status st, const char* fmt, ...);
 gq_status check_cuda(cudaError_t e, const char* what);
 
 // Colwise workspace layout: a 256-byte header (the ticket counter first),
-// then one done-counter per dependency group, then the amax words.  Offsets
-// in bytes; every region starts on a 256-byte boundary.
+// then one counter per 64 columns (the kernel uses one per 128-column slab),
+// then the (G, K) amax words.  Offsets in bytes; every region starts on a
+// 256-byte boundary.
 struct WorkspaceLayout {
-  size_t counters = 0;  // start of the done counters
+  size_t counters = 0;  // start of the counters
   size_t amax = 0;      // start of the amax words
   size_t total = 0;
 };
-WorkspaceLayout workspace_layout(int64_t dep_groups, int64_t amax_words);
+WorkspaceLayout colwise_workspace(int64_t K, int64_t G);
 
 namespace colwise {
 constexpr int kW = 128;  // columns per slab (dependency group)
