@@ -412,7 +412,8 @@ def run_mine(args):
                         f"10^U(-2,2)) + rowwise_t A {N}x{Mg} bf16, {Gr} groups "
                         "(2 empty, 0.5% outlier columns x1000)",
             "global_batch": M + Mg, "parallelism": f"replicas x{world}",
-            "l2": "inputs (512 MB, 272 MB) larger than L2 and disjoint; no flush",
+            "l2": f"inputs ({2 * M * K / 2**20:.0f} MiB, {2 * N * Mg / 2**20:.0f} MiB) larger "
+                  "than L2 and disjoint; no flush",
         },
         "per_call": {
             "colwise_us": col_avg * 1e3, "colwise_gbs": col_gbs,
