@@ -42,7 +42,7 @@ constexpr int kStages = 12;           // shared ring of stage buffers
 constexpr int kConsumerWarps = 4;
 constexpr int kSub = 8;               // stages per super tile
 constexpr int kSuper = kSub * kRows;  // rows per super tile
-constexpr int kCtx = 3;               // super-tile contexts in flight
+constexpr int kCtx = 2;               // super-tile contexts in flight
 // warps: consumers 0..3, producer 4, context 5, signal 6
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kContextWarp = kConsumerWarps + 1;
@@ -519,8 +519,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   const int64_t max_ctas =
       static_cast<int64_t>(info.sm_count) * info.colwise_ctas_per_sm;
   const int grid = static_cast<int>(total < max_ctas ? total : max_ctas);
-  p.sched.lag = schedule_lag(dbg.lag[GQ_KIND_COLWISE], p.sched.units, p.sched.groups,
-                             grid, kCtx);
+  p.sched.lag = schedule_lag(dbg.lag[GQ_KIND_COLWISE], p.sched.units, p.sched.groups, grid);
 
   const WorkspaceLayout L = colwise_workspace(K, G);
   uint8_t* w = static_cast<uint8_t*>(ws);

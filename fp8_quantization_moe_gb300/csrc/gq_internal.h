@@ -27,12 +27,10 @@ struct DebugKnobs {
   int32_t lag[2] = {0, 0};  // per kind; 0 = automatic
 };
 
-// The lag of the ticket order: `forced` if positive, else enough dependency
-// groups that a producer running `lead` tickets ahead of its consumers on
-// each of `grid` CTAs stays clear of phase-B tickets whose group is
-// unfinished; clamped to [1, groups].
-int32_t schedule_lag(int32_t forced, int64_t units, int64_t groups,
-                     int64_t grid, int lead);
+// The lag of the colwise ticket order: `forced` if positive, else the
+// number of slabs (of `units` tickets each) closest to a lead of 1.7
+// tickets per block of the `grid`; clamped to [1, groups].
+int32_t schedule_lag(int32_t forced, int64_t units, int64_t groups, int64_t grid);
 
 // Encodes a 2-D tiled tensor map (row-major, dim0 innermost).
 gq_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype,
