@@ -24,9 +24,10 @@
 // longer unit streams its windows twice through the ring, the second time
 // from L2 where it can.
 //
-// A producer warp claims units, publishes each in a small ring of unit
-// descriptors, and issues the TMA loads of the block's window stream into a
-// ring of kStages windows, kIssue windows side by side.  Pass A of a unit folds its amax, pass B scales,
+// A descriptor warp claims units and publishes each in a small ring of unit
+// descriptors; a loader warp follows the descriptors and issues the TMA
+// loads of the block's window stream into a ring of kStages windows, kIssue
+// windows side by side.  Pass A of a unit folds its amax, pass B scales,
 // casts and stores it; a pass covers the unit's windows in order.  Resident
 // units are visited with a lag of one unit,
 //   A(r0), A(r1), B(r0), A(r2), B(r1), ...,
@@ -72,8 +73,9 @@ constexpr int kUnits = 4;    // unit descriptors in flight
 constexpr int kConsumerWarps = 8;
 constexpr int kAhead = 2;  // units a block claims before it needs them
 constexpr int kIssue = 8;  // producer lanes issuing window loads side by side
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kLoaderWarp = kConsumerWarps;
+constexpr int kDescWarp = kConsumerWarps + 1;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kQ = kTn / 32;  // 32-row halves of a window
 constexpr int kStageBytes = kTn * kTm * 2;
 static_assert(kTm * 2 == 128 && kTn == 64, "128-byte swizzled rows, two 32-row halves");
@@ -89,7 +91,7 @@ struct Unit {
   int32_t nst;  // windows
   int32_t resident;  // 1: windows stay in the ring for pass B
   int32_t hold;      // test hook: the amax is never reported complete
-  uint32_t a_done;   // consumer warps through with pass A
+  uint32_t a_done;   // A visits finished
   alignas(16) uint32_t amax[kTn];  // row maxima, fp32 bit patterns
   alignas(16) float scale[kTn];    // written by the last warp through pass A
 };
@@ -119,7 +121,7 @@ struct Params {
   int32_t skip_arrival;
 };
 
-// --------------------------------------------------------- producer warp --
+// ------------------------------------------------- descriptor and loader --
 // Loads the nst windows of a pass (token columns x0 + 64 k, rows y ...) into
 // the ring: lanes 0 .. kIssue-1 take windows kb + lane side by side, each
 // waiting for its own slot.
@@ -144,19 +146,16 @@ __device__ __forceinline__ bool load_pass(Smem& s, const CUtensorMap* amap, uint
   return true;
 }
 
-__device__ __forceinline__ void producer_warp(Smem& s, const CUtensorMap* amap,
-                                              const Params& p, int lane) {
+// Claims units (kAhead ahead), decodes them and publishes their
+// descriptors; empty groups get their scales here and no descriptor.  The
+// whole warp builds the group-end table first.
+__device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int lane) {
   build_ends(p.offs, p.G, p.Mg, s.ends, lane);
   __syncwarp();
-  if (lane == 0) prefetch_tensormap(amap);
-  const uint64_t pol_once = policy_evict_first();  // read once
-  const uint64_t pol_again = policy_evict_last();  // a long unit's pass A
   const uint64_t wait_ns = 4 * p.timeout_ns;
-  uint32_t g = 0;     // loads issued
   uint32_t useq = 0;  // units published
-  bool ok = true;
   // lane 0 claims units kAhead ahead, so that a claim's round trip to L2
-  // overlaps the loads of the units before it
+  // overlaps the units before it
   uint32_t q[kAhead];
 #pragma unroll
   for (int a = 0; a < kAhead; ++a) q[a] = lane == 0 ? claim_ticket(p.ticket) : 0u;
@@ -183,10 +182,9 @@ __device__ __forceinline__ void producer_warp(Smem& s, const CUtensorMap* amap,
     }
     const int32_t x0 = s0 & ~7;
     const int nst = n0 >= 0 ? (e0 - x0 + kTm - 1) / kTm : 0;
-    const bool resident = nst <= kFit;
     const int us = static_cast<int>(useq % kUnits);
-    ok = mbar_wait(&s.u_free[us], ((useq / kUnits) & 1) ^ 1u, wait_ns, p.err);
-    if (__any_sync(0xffffffffu, !ok)) break;
+    const bool ok = mbar_wait(&s.u_free[us], ((useq / kUnits) & 1) ^ 1u, wait_ns, p.err);
+    if (__any_sync(0xffffffffu, !ok)) return;
     Unit& U = s.unit[us];
     if (lane < kTn / 4) sts128(smem_addr(&U.amax[4 * lane]), make_uint4(0, 0, 0, 0));
     if (lane == 0) {
@@ -196,17 +194,38 @@ __device__ __forceinline__ void producer_warp(Smem& s, const CUtensorMap* amap,
       U.lo = s0 - x0;
       U.hi = e0 - x0;
       U.nst = nst;
-      U.resident = resident ? 1 : 0;
+      U.resident = nst <= kFit ? 1 : 0;
       U.hold = p.skip_arrival && u == 0u;
       U.a_done = 0u;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.u_full[us]);
     ++useq;
-    // the stream's loads: pass A of the unit; a long unit's pass B at once
+    if (n0 < 0) return;
+  }
+}
+
+// Follows the published descriptors and loads the window stream: pass A of
+// each unit, and a long unit's pass B at once.
+__device__ __forceinline__ void loader_warp(Smem& s, const CUtensorMap* amap, const Params& p,
+                                            int lane) {
+  if (lane == 0) prefetch_tensormap(amap);
+  const uint64_t pol_once = policy_evict_first();  // read once
+  const uint64_t pol_again = policy_evict_last();  // a long unit's pass A
+  const uint64_t wait_ns = 4 * p.timeout_ns;
+  uint32_t g = 0;  // loads issued
+  for (uint32_t useq = 0;; ++useq) {
+    const int us = static_cast<int>(useq % kUnits);
+    bool ok = mbar_wait(&s.u_full[us], (useq / kUnits) & 1, wait_ns, p.err);
+    if (__any_sync(0xffffffffu, !ok)) break;
+    const Unit& U = s.unit[us];
+    const int32_t n0 = U.n0, x0 = U.x0;
+    const int nst = U.nst;
+    const bool resident = U.resident != 0;
+    if (n0 < 0) break;
     ok = load_pass(s, amap, g, nst, x0, n0, resident ? pol_once : pol_again, lane, wait_ns, p.err);
     if (ok && !resident) ok = load_pass(s, amap, g, nst, x0, n0, pol_once, lane, wait_ns, p.err);
-    if (!ok || n0 < 0) break;
+    if (!ok) break;
   }
   // no load may still be in flight when the block exits
   if (lane == 0)
@@ -352,13 +371,15 @@ __device__ __forceinline__ bool wait_load(Smem& s, uint32_t ld, uint64_t wait_ns
 }
 
 // Pass A of unit `cu` (its windows are ring loads cu.first ...): this warp's
-// visits, then its arrival on the unit's amax barrier.
+// visits, and from the warp finishing the last of them the unit's scales.
 __device__ __forceinline__ bool pass_a(Smem& s, const UnitView& cu, bool hold, uint32_t& j,
                                        const Params& p, int w, int lane, uint64_t wait_ns) {
   unsigned* err = p.err;
   Unit& U = s.unit[cu.useq % kUnits];
-  for (int k = static_cast<int>((w + kConsumerWarps - j % kConsumerWarps) % kConsumerWarps);
-       k < cu.nst; k += kConsumerWarps) {
+  const int k0 = static_cast<int>((w + kConsumerWarps - j % kConsumerWarps) % kConsumerWarps);
+  j += static_cast<uint32_t>(cu.nst);
+  if (k0 >= cu.nst) return true;  // no visit of this unit
+  for (int k = k0; k < cu.nst; k += kConsumerWarps) {
     const uint32_t ld = cu.first + k;
     const bool ok = wait_load(s, ld, wait_ns, err);
     if (__any_sync(0xffffffffu, !ok)) return false;
@@ -369,14 +390,14 @@ __device__ __forceinline__ bool pass_a(Smem& s, const UnitView& cu, bool hold, u
       if (lane == 0) mbar_arrive(&s.empty[ld % kStages]);
     }
   }
-  j += static_cast<uint32_t>(cu.nst);
-  // the last warp through pass A (an acquire-release counter says which)
-  // turns the amax words into the unit's scales, once
+  // the warp that finishes the unit's last A visit (an acquire-release
+  // counter of visits says which) turns the amax words into its scales, once
+  const uint32_t mine = static_cast<uint32_t>((cu.nst - k0 + kConsumerWarps - 1) / kConsumerWarps);
   __syncwarp();
   uint32_t prev = 0;
-  if (lane == 0) prev = atom_add_acq_rel_cta_shared(smem_addr(&U.a_done), 1u);
+  if (lane == 0) prev = atom_add_acq_rel_cta_shared(smem_addr(&U.a_done), mine);
   prev = __shfl_sync(0xffffffffu, prev, 0);
-  if (prev + 1 == static_cast<uint32_t>(kConsumerWarps)) {
+  if (prev + mine == static_cast<uint32_t>(cu.nst)) {
 #pragma unroll
     for (int qq = 0; qq < kQ; ++qq) {
       const int r = lane + 32 * qq;
@@ -484,8 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  if (warp == kProducerWarp)
-    producer_warp(s, &amap, p, lane);
+  if (warp == kDescWarp)
+    descriptor_warp(s, p, lane);
+  else if (warp == kLoaderWarp)
+    loader_warp(s, &amap, p, lane);
   else
     consumer_warp(s, p, warp, lane);
 }
