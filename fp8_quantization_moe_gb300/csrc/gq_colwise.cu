@@ -384,15 +384,14 @@ __device__ __forceinline__ void stage_b(Smem& s, const Ctx& c, int k, uint32_t t
     sc[7] = __shfl_sync(0xffffffffu, s3, l1);
     if (!chunk_in) continue;
     if (ra <= 0 && rb >= kRows) {
+      // all of the lane's rows: loads first, then the casts and stores, so
+      // that sixteen independent chains hide the latency of each step
+      uint4 v[kRows / 2];
 #pragma unroll
-      for (int hb = 0; hb < kRows / 16; ++hb) {  // batches of 8 rows: loads first
-        uint4 v[8];
+      for (int i = 0; i < kRows / 2; ++i) v[i] = lds128(base + i * 2 * kRowBytes);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = lds128(base + (hb * 8 + i) * 2 * kRowBytes);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          __stcs(reinterpret_cast<uint2*>(obase + (hb * 8 + i) * K2), quant8(v[i], sc));
-      }
+      for (int i = 0; i < kRows / 2; ++i)
+        __stcs(reinterpret_cast<uint2*>(obase + i * K2), quant8(v[i], sc));
     } else {
 #pragma unroll 1
       for (int i = 0; i < kRows / 2; ++i) {
