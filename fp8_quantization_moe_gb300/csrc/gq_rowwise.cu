@@ -15,7 +15,7 @@
 // Work unit: one (row band, group) pair -- kTn = 64 rows of A by the group's
 // token columns.  Every scale of the unit depends on the unit alone, so no
 // block ever waits for another: a persistent grid claims units from a global
-// counter, band by band.  A unit is read through windows of kTn rows x kTm =
+// counter, group by group.  A unit is read through windows of kTn rows x kTm =
 // 64 token columns (8 KB, one TMA box with the 128-byte swizzle, so that
 // row-wise and column-wise shared-memory accesses are bank-conflict free);
 // window 0 starts at s_g rounded down to 8 tokens (the TMA's 16-byte rule).
@@ -117,6 +117,7 @@ struct Params {
   unsigned* err;
   int32_t N, Mg, G;
   uint32_t units;  // row bands x groups
+  uint32_t bands;  // row bands of kTn rows
   uint64_t timeout_ns;
   int32_t skip_arrival;
 };
@@ -166,8 +167,11 @@ __device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int la
     if (lane == 0 && u < p.units) q[kAhead - 1] = claim_ticket(p.ticket);
     int32_t grp = 0, n0 = -1, s0 = 0, e0 = 0;
     if (u < p.units) {  // else: publish the stop descriptor
-      grp = static_cast<int32_t>(u % static_cast<uint32_t>(p.G));
-      n0 = static_cast<int32_t>(u / static_cast<uint32_t>(p.G)) * kTn;
+      // group-major: the bands of a group are claimed one after another, so
+      // the 64-byte runs that neighbouring bands write into each row of A^T
+      // reach L2 close together
+      grp = static_cast<int32_t>(u / static_cast<uint32_t>(p.bands));
+      n0 = static_cast<int32_t>(u % static_cast<uint32_t>(p.bands)) * kTn;
       s0 = grp ? s.ends[grp - 1] : 0;
       e0 = s.ends[grp];
       if (e0 == s0) {  // empty group: amax 0 for every row
@@ -559,6 +563,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
   p.Mg = Mg;
   p.G = G;
   p.units = static_cast<uint32_t>(units);
+  p.bands = static_cast<uint32_t>(bands);
   p.timeout_ns = dbg.timeout_ns;
   p.skip_arrival = dbg.skip_arrival;
 
