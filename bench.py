@@ -49,6 +49,7 @@ PAGES_CONTEXT = {
     "rowwise_16640x8192_g64_triton_transpose_us": 784.288,
     "source": "pytorch/ao #2668 new-autotune table; #2863 Benchmarks table",
 }
+POW2 = False  # --pow2-scales
 KERNEL_SOURCES = ["gq_device.cuh", "gq_colwise.cu", "gq_rowwise.cu"]
 
 
@@ -303,8 +304,8 @@ def run_mine(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        gq.colwise(x, xo, out=q, scales=qs, stream=stream)
-        gq.rowwise_t(a, ao, out=qt, scales=ts, stream=stream)
+        gq.colwise(x, xo, out=q, scales=qs, stream=stream, pow2_scales=POW2)
+        gq.rowwise_t(a, ao, out=qt, scales=ts, stream=stream, pow2_scales=POW2)
 
     props = torch.cuda.get_device_properties(dev)
     sampler = ClockSampler(f"GPU-{props.uuid}")
@@ -331,9 +332,9 @@ def run_mine(args):
           for _ in range(args.steps)]
     for i in range(args.steps):
         ev[i][0].record(stream)
-        gq.colwise(x, xo, out=q, scales=qs, stream=stream)
+        gq.colwise(x, xo, out=q, scales=qs, stream=stream, pow2_scales=POW2)
         ev[i][1].record(stream)
-        gq.rowwise_t(a, ao, out=qt, scales=ts, stream=stream)
+        gq.rowwise_t(a, ao, out=qt, scales=ts, stream=stream, pow2_scales=POW2)
         ev[i][2].record(stream)
     torch.cuda.synchronize(dev)
     if dist_ok:
@@ -361,8 +362,8 @@ def run_mine(args):
     tsh = torch.empty((N, Gr), dtype=torch.float32, pin_memory=True)
 
     def e2e_step():
-        gq.colwise_host(xh, xoh, qh, qsh, device=dev, stream=stream)
-        gq.rowwise_t_host(ah, aoh, qth, tsh, device=dev, stream=stream)
+        gq.colwise_host(xh, xoh, qh, qsh, device=dev, stream=stream, pow2_scales=POW2)
+        gq.rowwise_t_host(ah, aoh, qth, tsh, device=dev, stream=stream, pow2_scales=POW2)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -412,6 +413,7 @@ def run_mine(args):
                         f"10^U(-2,2)) + rowwise_t A {N}x{Mg} bf16, {Gr} groups "
                         "(2 empty, 0.5% outlier columns x1000)",
             "global_batch": M + Mg, "parallelism": f"replicas x{world}",
+            "scales": "rounded down to powers of two" if POW2 else "448 / max(amax, 1e-12)",
             "l2": f"inputs ({2 * M * K / 2**20:.0f} MiB, {2 * N * Mg / 2**20:.0f} MiB) larger "
                   "than L2 and disjoint; no flush",
         },
@@ -462,11 +464,16 @@ def main(argv=None):
     ap.add_argument("--clock-window", type=float, default=1.5,
                     help="seconds of sustained load around the timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pow2-scales", action="store_true",
+                    help="round every scale down to a power of two (the "
+                         "round_scales_to_power_of_2 option); same bytes moved")
     ap.add_argument("--half", action="store_true",
                     help="profiling case: half the tokens of each workload "
                          "(inputs 256 MB and 136 MB, still larger than L2); "
                          "not the benchmark configuration")
     args = ap.parse_args(argv)
+    global POW2
+    POW2 = bool(args.pow2_scales)
     if args.half:
         global COLWISE_SHAPE, ROWWISE_SHAPE
         COLWISE_SHAPE = (COLWISE_SHAPE[0] // 2,) + COLWISE_SHAPE[1:]

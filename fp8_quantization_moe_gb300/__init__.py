@@ -8,12 +8,13 @@ Two paths, both in hand-written sm_103a CUDA kernels behind the C ABI of
   output written transposed.
 
 scale = 448 / max(amax, 1e-12) in IEEE fp32; q = saturating round-to-nearest-
-even e4m3 cast of fp32(x * scale).  ``offs`` are int32 end offsets of the
+even e4m3 cast of fp32(x * scale); ``pow2_scales=True`` rounds every scale
+down to a power of two first.  ``offs`` are int32 end offsets of the
 token groups.  This package is argument marshalling over the library; torch
 supplies device memory and streams.  ``synth`` draws seeded inputs.
 """
 from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
-                       GQError, check_device_error, colwise, colwise_host,
+                       GQ_SCALE_POW2, GQError, check_device_error, colwise, colwise_host,
                        colwise_noalloc,
                        debug_set, lib, library_path, rowwise_t,
                        rowwise_t_host, set_lag, status_string, version,
@@ -21,7 +22,7 @@ from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
 from ._build import build
 
 __all__ = [
-    "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQError",
+    "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQ_SCALE_POW2", "GQError",
     "build", "check_device_error", "colwise", "colwise_host",
     "colwise_noalloc", "debug_set",
     "lib", "library_path", "rowwise_t", "rowwise_t_host", "set_lag",

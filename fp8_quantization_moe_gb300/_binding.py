@@ -23,6 +23,7 @@ GQ_ERR_TIMEOUT = 4
 GQ_KIND_COLWISE = 0
 GQ_KIND_ROWWISE_T = 1
 GQ_MAX_GROUPS = 1024
+GQ_SCALE_POW2 = 1
 
 # Every symbol the header declares, with its ctypes signature.
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
@@ -31,6 +32,8 @@ SIGNATURES = {
     "gq_fp8_colwise": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "gq_fp8_rowwise_t": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "gq_fp8_colwise_noalloc": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P]),
+    "gq_fp8_colwise_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
+    "gq_fp8_rowwise_t_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
     "gq_check_device_error": (ctypes.c_int, [_P]),
     "gq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gq_last_error": (ctypes.c_char_p, []),
@@ -148,8 +151,11 @@ def _check_in(x, offs, name):
 # ---------------------------------------------------------------- paths --
 
 def colwise(x: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
-            stream=None, workspace=None):
+            stream=None, workspace=None, pow2_scales: bool = False):
     """Colwise per-token-group scaling (groups along dim0).
+
+    ``pow2_scales`` rounds every scale down to a power of two
+    (GQ_SCALE_POW2).
 
     x: bf16 (M, K) CUDA tensor; offs: int32 (n_groups,) end offsets on the
     same device.  Returns (q float8_e4m3fn (M, K), scales float32
@@ -174,16 +180,17 @@ def colwise(x: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
     ws = workspace if workspace is not None else _workspace(need, dev, sh)
     wp, wn = _ws_ptr(ws)
     with torch.cuda.device(dev):
-        st = lib().gq_fp8_colwise(_ptr(x), M, K, _ptr(offs), G, _ptr(out),
-                                  _ptr(scales), wp, wn, sh)
+        st = lib().gq_fp8_colwise_ex(_ptr(x), M, K, _ptr(offs), G, _ptr(out),
+                                     _ptr(scales), GQ_SCALE_POW2 if pow2_scales else 0,
+                                     wp, wn, sh)
     _check(st, "gq_fp8_colwise")
     return out, scales
 
 
 def rowwise_t(a: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
-              stream=None, workspace=None):
+              stream=None, workspace=None, pow2_scales: bool = False):
     """Rowwise per-token-group scaling with transposed output (groups along
-    dim1 of A).
+    dim1 of A).  ``pow2_scales`` rounds every scale down to a power of two.
 
     a: bf16 (N, Mg) CUDA tensor; offs: int32 (n_groups,) end offsets along
     Mg.  Returns (qt float8_e4m3fn (Mg, N) = q(a)^T, scales float32
@@ -206,8 +213,9 @@ def rowwise_t(a: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
     ws = workspace if workspace is not None else _workspace(need, dev, sh)
     wp, wn = _ws_ptr(ws)
     with torch.cuda.device(dev):
-        st = lib().gq_fp8_rowwise_t(_ptr(a), N, Mg, _ptr(offs), G, _ptr(out),
-                                    _ptr(scales), wp, wn, sh)
+        st = lib().gq_fp8_rowwise_t_ex(_ptr(a), N, Mg, _ptr(offs), G, _ptr(out),
+                                       _ptr(scales), GQ_SCALE_POW2 if pow2_scales else 0,
+                                       wp, wn, sh)
     _check(st, "gq_fp8_rowwise_t")
     return out, scales
 
@@ -269,7 +277,7 @@ def _to_device(t, device, name):
 
 
 def colwise_host(x_host, offs_host, out_host=None, scales_host=None, *,
-                 device="cuda", stream=None):
+                 device="cuda", stream=None, pow2_scales: bool = False):
     """End-to-end colwise call on host buffers: host->device copies of x and
     offs, the kernel, device->host copies of q and scales, all enqueued on
     ``stream``.  Pinned host tensors make the copies asynchronous; the caller
@@ -285,14 +293,14 @@ def colwise_host(x_host, offs_host, out_host=None, scales_host=None, *,
     with torch.cuda.stream(s):
         x = _to_device(x_host, dev, "colwise_host")
         o = _to_device(offs_host, dev, "colwise_host")
-        q, sc = colwise(x, o, stream=s)
+        q, sc = colwise(x, o, stream=s, pow2_scales=pow2_scales)
         out_host.copy_(q, non_blocking=True)
         scales_host.copy_(sc, non_blocking=True)
     return out_host, scales_host
 
 
 def rowwise_t_host(a_host, offs_host, out_host=None, scales_host=None, *,
-                   device="cuda", stream=None):
+                   device="cuda", stream=None, pow2_scales: bool = False):
     """End-to-end rowwise_t call on host buffers (see colwise_host)."""
     dev = torch.device(device)
     N, Mg = a_host.shape
@@ -305,7 +313,7 @@ def rowwise_t_host(a_host, offs_host, out_host=None, scales_host=None, *,
     with torch.cuda.stream(s):
         a = _to_device(a_host, dev, "rowwise_t_host")
         o = _to_device(offs_host, dev, "rowwise_t_host")
-        qt, sc = rowwise_t(a, o, stream=s)
+        qt, sc = rowwise_t(a, o, stream=s, pow2_scales=pow2_scales)
         out_host.copy_(qt, non_blocking=True)
         scales_host.copy_(sc, non_blocking=True)
     return out_host, scales_host

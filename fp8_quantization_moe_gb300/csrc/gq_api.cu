@@ -162,10 +162,16 @@ WorkspaceLayout colwise_workspace(int64_t K, int64_t G) {
   return L;
 }
 
-gq_status launch_fill_empty_scales(float* scales, int64_t n,
+gq_status launch_fill_empty_scales(float* scales, int64_t n, uint32_t flags,
                                    cudaStream_t stream) {
   if (n <= 0) return GQ_OK;
-  const float v = kFp8Max / kEps;  // IEEE fp32 division on the host
+  float v = kFp8Max / kEps;  // IEEE fp32 division on the host
+  if (flags & GQ_SCALE_POW2) {  // the power of two below: clear the mantissa
+    uint32_t b;
+    memcpy(&b, &v, sizeof b);
+    b &= 0xFF800000u;
+    memcpy(&v, &b, sizeof v);
+  }
   const int threads = 256;
   const int64_t blocks64 = (n + threads - 1) / threads;
   const int blocks = static_cast<int>(blocks64 < 4096 ? blocks64 : 4096);
@@ -178,6 +184,8 @@ gq_status launch_fill_empty_scales(float* scales, int64_t n,
 using namespace gq;
 
 namespace {
+
+constexpr uint32_t kKnownFlags = GQ_SCALE_POW2;
 
 gq_status validate_common(const void* in, const void* out, const int32_t* offs,
                           int32_t n_groups, const float* scales, int64_t rows,
@@ -241,7 +249,17 @@ gq_status gq_fp8_colwise(const void* x, int64_t M, int64_t K,
                          const int32_t* offs, int32_t n_groups, void* out,
                          float* scales, void* workspace,
                          size_t workspace_bytes, gq_stream_t stream) {
+  return gq_fp8_colwise_ex(x, M, K, offs, n_groups, out, scales, 0u, workspace,
+                           workspace_bytes, stream);
+}
+
+gq_status gq_fp8_colwise_ex(const void* x, int64_t M, int64_t K,
+                            const int32_t* offs, int32_t n_groups, void* out,
+                            float* scales, uint32_t flags, void* workspace,
+                            size_t workspace_bytes, gq_stream_t stream) {
   const char* name = "gq_fp8_colwise";
+  if (flags & ~kKnownFlags)
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kKnownFlags);
   gq_status st = validate_common(x, out, offs, n_groups, scales, M, K, name);
   if (st != GQ_OK) return st;
   if (K % 16 != 0)
@@ -258,17 +276,27 @@ gq_status gq_fp8_colwise(const void* x, int64_t M, int64_t K,
   if (st != GQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (M == 0)
-    return launch_fill_empty_scales(scales, static_cast<int64_t>(n_groups) * K, s);
+    return launch_fill_empty_scales(scales, static_cast<int64_t>(n_groups) * K, flags, s);
   return colwise::launch(*info, g_dbg, x, static_cast<int32_t>(M),
                          static_cast<int32_t>(K), offs, n_groups, out, scales,
-                         workspace, s);
+                         flags, workspace, s);
 }
 
 gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,
                            const int32_t* offs, int32_t n_groups, void* out_t,
                            float* scales, void* workspace,
                            size_t workspace_bytes, gq_stream_t stream) {
+  return gq_fp8_rowwise_t_ex(a, N, Mg, offs, n_groups, out_t, scales, 0u, workspace,
+                             workspace_bytes, stream);
+}
+
+gq_status gq_fp8_rowwise_t_ex(const void* a, int64_t N, int64_t Mg,
+                              const int32_t* offs, int32_t n_groups, void* out_t,
+                              float* scales, uint32_t flags, void* workspace,
+                              size_t workspace_bytes, gq_stream_t stream) {
   const char* name = "gq_fp8_rowwise_t";
+  if (flags & ~kKnownFlags)
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kKnownFlags);
   gq_status st = validate_common(a, out_t, offs, n_groups, scales, N, Mg, name);
   if (st != GQ_OK) return st;
   if (N % 16 != 0)
@@ -288,10 +316,10 @@ gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,
   if (st != GQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (Mg == 0)
-    return launch_fill_empty_scales(scales, N * static_cast<int64_t>(n_groups), s);
+    return launch_fill_empty_scales(scales, N * static_cast<int64_t>(n_groups), flags, s);
   return rowwise::launch(*info, g_dbg, a, static_cast<int32_t>(N),
                          static_cast<int32_t>(Mg), offs, n_groups, out_t, scales,
-                         workspace, s);
+                         flags, workspace, s);
 }
 
 gq_status gq_check_device_error(gq_stream_t stream) {

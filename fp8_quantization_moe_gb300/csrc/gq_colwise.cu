@@ -104,6 +104,7 @@ struct Params {
   Schedule sched;  // units = super tiles per slab
   uint64_t timeout_ns;
   int32_t skip_arrival;
+  bool pow2;  // scales rounded down to powers of two
 };
 
 // Shared-memory offset of chunk k (0..15, 8 columns each) of stage row r.
@@ -339,7 +340,7 @@ __device__ __forceinline__ void stage_b(Smem& s, const Ctx& c, int k, uint32_t t
     for (int g = h.own_lo; g < h.own_hi; ++g) {
       const int32_t gs = g ? s.ends[g - 1] : 0;
       if (c4_in && s.ends[g] == gs) {
-        const float e = scale_from_amax_bits(0u);
+        const float e = scale_from_amax_bits(0u, p.pow2);
         *reinterpret_cast<float4*>(p.scales + static_cast<size_t>(g) * p.K + c4) =
             make_float4(e, e, e, e);
       }
@@ -365,8 +366,8 @@ __device__ __forceinline__ void stage_b(Smem& s, const Ctx& c, int k, uint32_t t
     } else {
       am = make_uint4(0u, 0u, 0u, 0u);
     }
-    const float s0 = scale_from_amax_bits(am.x), s1 = scale_from_amax_bits(am.y);
-    const float s2 = scale_from_amax_bits(am.z), s3 = scale_from_amax_bits(am.w);
+    const float s0 = scale_from_amax_bits(am.x, p.pow2), s1 = scale_from_amax_bits(am.y, p.pow2);
+    const float s2 = scale_from_amax_bits(am.z, p.pow2), s3 = scale_from_amax_bits(am.w, p.pow2);
     // the group starts inside the super tile at row seg_lo: the stage
     // holding that row writes its scales
     if (ra >= 0 && c4_in && g >= h.own_lo && g < h.own_hi)
@@ -502,7 +503,7 @@ gq_status setup(DeviceInfo& info) {
 
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
                  int32_t M, int32_t K, const int32_t* offs, int32_t G,
-                 void* out, float* scales, void* ws, cudaStream_t stream) {
+                 void* out, float* scales, uint32_t flags, void* ws, cudaStream_t stream) {
   CUtensorMap xmap;
   gq_status st = encode_tiled_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                  const_cast<void*>(x), static_cast<uint64_t>(K),
@@ -534,6 +535,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   p.G = G;
   p.timeout_ns = dbg.timeout_ns;
   p.skip_arrival = dbg.skip_arrival;
+  p.pow2 = (flags & GQ_SCALE_POW2) != 0;
 
   st = check_cuda(cudaMemsetAsync(ws, 0, L.total, stream), "colwise: clear workspace");
   if (st != GQ_OK) return st;

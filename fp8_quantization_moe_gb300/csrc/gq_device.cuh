@@ -343,6 +343,14 @@ __device__ __forceinline__ float scale_from_amax_bits(uint32_t bits) {
   return __fdiv_rn(kFp8Max, fmaxf(a, kEps));
 }
 
+// The same scale, rounded down to a power of two when `pow2` is set
+// (round_scales_to_power_of_2): the scale is a positive normal fp32
+// (448 / 3.4e38 > 2^-126), so clearing its mantissa leaves 2^floor(log2 s).
+__device__ __forceinline__ float scale_from_amax_bits(uint32_t bits, bool pow2) {
+  const float s = scale_from_amax_bits(bits);
+  return pow2 ? __uint_as_float(__float_as_uint(s) & 0xFF800000u) : s;
+}
+
 __device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) {
   return __ldcg(p);
 }

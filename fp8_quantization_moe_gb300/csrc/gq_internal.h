@@ -60,7 +60,7 @@ constexpr int kW = 128;  // columns per slab (dependency group)
 gq_status setup(DeviceInfo& info);
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
                  int32_t M, int32_t K, const int32_t* offs, int32_t G,
-                 void* out, float* scales, void* ws, cudaStream_t stream);
+                 void* out, float* scales, uint32_t flags, void* ws, cudaStream_t stream);
 }  // namespace colwise
 
 namespace rowwise {
@@ -70,12 +70,13 @@ constexpr size_t kWorkspaceBytes = 256;  // the unit counter, padded
 gq_status setup(DeviceInfo& info);
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
                  int32_t N, int32_t Mg, const int32_t* offs, int32_t G,
-                 void* out_t, float* scales, void* ws, cudaStream_t stream);
+                 void* out_t, float* scales, uint32_t flags, void* ws, cudaStream_t stream);
 }  // namespace rowwise
 
-// Writes 448 / 1e-12 (fp32) into n scales: every group is empty when the
-// token extent is 0.
-gq_status launch_fill_empty_scales(float* scales, int64_t n,
+// Writes the scale of an empty group -- 448 / 1e-12 (fp32), or its power
+// of two below with GQ_SCALE_POW2 -- into n scales: every group is empty
+// when the token extent is 0.
+gq_status launch_fill_empty_scales(float* scales, int64_t n, uint32_t flags,
                                    cudaStream_t stream);
 
 }  // namespace gq

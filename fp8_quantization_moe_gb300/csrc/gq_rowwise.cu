@@ -120,6 +120,7 @@ struct Params {
   uint32_t bands;  // row bands of kTn rows
   uint64_t timeout_ns;
   int32_t skip_arrival;
+  bool pow2;  // scales rounded down to powers of two
 };
 
 // ------------------------------------------------- descriptor and loader --
@@ -175,7 +176,7 @@ __device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int la
       s0 = grp ? s.ends[grp - 1] : 0;
       e0 = s.ends[grp];
       if (e0 == s0) {  // empty group: amax 0 for every row
-        const float e = scale_from_amax_bits(0u);
+        const float e = scale_from_amax_bits(0u, p.pow2);
 #pragma unroll
         for (int qq = 0; qq < kQ; ++qq) {
           const int32_t n = n0 + lane + 32 * qq;
@@ -405,7 +406,7 @@ __device__ __forceinline__ bool pass_a(Smem& s, const UnitView& cu, bool hold, u
 #pragma unroll
     for (int qq = 0; qq < kQ; ++qq) {
       const int r = lane + 32 * qq;
-      const float sc = scale_from_amax_bits(U.amax[r]);
+      const float sc = scale_from_amax_bits(U.amax[r], p.pow2);
       U.scale[r] = sc;
       if (cu.n0 + r < p.N) p.scales[static_cast<size_t>(cu.n0 + r) * p.G + cu.g] = sc;
     }
@@ -537,7 +538,7 @@ gq_status setup(DeviceInfo& info) {
 
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
                  int32_t N, int32_t Mg, const int32_t* offs, int32_t G,
-                 void* out_t, float* scales, void* ws, cudaStream_t stream) {
+                 void* out_t, float* scales, uint32_t flags, void* ws, cudaStream_t stream) {
   CUtensorMap amap;
   gq_status st = encode_tiled_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                  const_cast<void*>(a), static_cast<uint64_t>(Mg),
@@ -566,6 +567,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
   p.bands = static_cast<uint32_t>(bands);
   p.timeout_ns = dbg.timeout_ns;
   p.skip_arrival = dbg.skip_arrival;
+  p.pow2 = (flags & GQ_SCALE_POW2) != 0;
 
   st = check_cuda(cudaMemsetAsync(ws, 0, 4, stream), "rowwise_t: clear unit counter");
   if (st != GQ_OK) return st;

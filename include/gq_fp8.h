@@ -135,6 +135,32 @@ gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,
                            size_t workspace_bytes, gq_stream_t stream);
 
 /*
+ * Options of the _ex calls (a bit mask; unknown bits are GQ_ERR_INVALID_ARG).
+ *   GQ_SCALE_POW2  round every scale down to a power of two,
+ *                  s = 2^floor(log2(448 / max(amax, 1e-12))) -- the
+ *                  round_scales_to_power_of_2 option of the kernel in
+ *                  pytorch/ao #2668 (kernel arguments in its torch.compile
+ *                  failure report).  The cast multiplies by s as usual; the
+ *                  product is then exact, and the scale no larger than the
+ *                  plain one, so in a group column (row) whose amax is at
+ *                  least 1e-12 the largest |q| lies in [224, 448].
+ */
+#define GQ_SCALE_POW2 1u
+
+/*
+ * gq_fp8_colwise / gq_fp8_rowwise_t with option flags; the calls above are
+ * these with flags = 0.  Arguments, layouts and errors as above.
+ */
+gq_status gq_fp8_colwise_ex(const void* x, int64_t M, int64_t K,
+                            const int32_t* offs, int32_t n_groups, void* out,
+                            float* scales, uint32_t flags, void* workspace,
+                            size_t workspace_bytes, gq_stream_t stream);
+gq_status gq_fp8_rowwise_t_ex(const void* a, int64_t N, int64_t Mg,
+                              const int32_t* offs, int32_t n_groups, void* out_t,
+                              float* scales, uint32_t flags, void* workspace,
+                              size_t workspace_bytes, gq_stream_t stream);
+
+/*
  * Colwise scaling with no allocation at all, not even a caller workspace.
  * The pytorch/ao pages have no counterpart to this entry point; it exists for
  * callers that cannot obtain device memory at the point where they quantize

@@ -60,6 +60,12 @@ class Oracle:
         lib.gqo_colwise.restype = ctypes.c_int
         lib.gqo_rowwise_t.argtypes = [p, i64, i64, p, i32, p, p]
         lib.gqo_rowwise_t.restype = ctypes.c_int
+        lib.gqo_colwise_ex.argtypes = [p, i64, i64, p, i32, ctypes.c_int, p, p]
+        lib.gqo_colwise_ex.restype = ctypes.c_int
+        lib.gqo_rowwise_t_ex.argtypes = [p, i64, i64, p, i32, ctypes.c_int, p, p]
+        lib.gqo_rowwise_t_ex.restype = ctypes.c_int
+        lib.gqo_scale_pow2_array.argtypes = [p, i64, p]
+        lib.gqo_scale_pow2_array.restype = None
         lib.gqo_e4m3_encode_array.argtypes = [p, i64, p]
         lib.gqo_e4m3_decode_array.argtypes = [p, i64, p]
         lib.gqo_scale_array.argtypes = [p, i64, p]
@@ -92,6 +98,13 @@ class Oracle:
         self.lib.gqo_scale_array(a.ctypes.data, a.size, out.ctypes.data)
         return out
 
+    def scale_pow2_of(self, amax) -> np.ndarray:
+        """2^floor(log2(448 / max(amax, 1e-12))) for an array of fp32 amax."""
+        a = _c(amax, np.float32)
+        out = np.empty(a.shape, np.float32)
+        self.lib.gqo_scale_pow2_array(a.ctypes.data, a.size, out.ctypes.data)
+        return out
+
     def quant(self, x_bf16_bits, scale) -> np.ndarray:
         """Elementwise e4m3(fp32(x * scale)); x as bf16 bit patterns."""
         x = _c(x_bf16_bits, np.uint16)
@@ -103,12 +116,13 @@ class Oracle:
         return out
 
     # ---------------------------------------------------------------- paths
-    def colwise(self, x_bf16_bits, offs, out=None):
+    def colwise(self, x_bf16_bits, offs, out=None, pow2=False):
         """Per-group scaling along dim0.
 
         x: uint16 (M, K) bf16 bits, row-major.  offs: int32 end offsets.
         Returns (q uint8 (M, K), scales float32 (n_groups, K)).  Rows outside
         every group keep the value of ``out`` (zeros when ``out`` is None).
+        ``pow2`` rounds every scale down to a power of two.
         """
         x = _c(x_bf16_bits, np.uint16)
         assert x.ndim == 2
@@ -116,14 +130,15 @@ class Oracle:
         M, K = x.shape
         q = np.zeros((M, K), np.uint8) if out is None else _c(out, np.uint8).copy()
         s = np.empty((o.size, K), np.float32)
-        rc = self.lib.gqo_colwise(x.ctypes.data, M, K, o.ctypes.data, o.size,
-                                  q.ctypes.data, s.ctypes.data)
+        rc = self.lib.gqo_colwise_ex(x.ctypes.data, M, K, o.ctypes.data, o.size,
+                                     int(bool(pow2)), q.ctypes.data, s.ctypes.data)
         if rc != 0:
             raise ValueError("oracle colwise: invalid arguments")
         return q, s
 
-    def rowwise_t(self, a_bf16_bits, offs, out=None):
-        """Per-group scaling along dim1 with transposed output.
+    def rowwise_t(self, a_bf16_bits, offs, out=None, pow2=False):
+        """Per-group scaling along dim1 with transposed output (``pow2``:
+        scales rounded down to powers of two).
 
         a: uint16 (N, Mg) bf16 bits, row-major.  offs: int32 end offsets
         along Mg.  Returns (qt uint8 (Mg, N) = q(a)^T, scales float32
@@ -135,8 +150,9 @@ class Oracle:
         N, Mg = a.shape
         qt = np.zeros((Mg, N), np.uint8) if out is None else _c(out, np.uint8).copy()
         s = np.empty((N, o.size), np.float32)
-        rc = self.lib.gqo_rowwise_t(a.ctypes.data, N, Mg, o.ctypes.data,
-                                    o.size, qt.ctypes.data, s.ctypes.data)
+        rc = self.lib.gqo_rowwise_t_ex(a.ctypes.data, N, Mg, o.ctypes.data,
+                                       o.size, int(bool(pow2)), qt.ctypes.data,
+                                       s.ctypes.data)
         if rc != 0:
             raise ValueError("oracle rowwise_t: invalid arguments")
         return qt, s
@@ -171,12 +187,16 @@ def quant(x_bf16_bits, scale):
     return get().quant(x_bf16_bits, scale)
 
 
-def colwise(x_bf16_bits, offs, out=None):
-    return get().colwise(x_bf16_bits, offs, out)
+def scale_pow2_of(amax):
+    return get().scale_pow2_of(amax)
 
 
-def rowwise_t(a_bf16_bits, offs, out=None):
-    return get().rowwise_t(a_bf16_bits, offs, out)
+def colwise(x_bf16_bits, offs, out=None, pow2=False):
+    return get().colwise(x_bf16_bits, offs, out, pow2)
+
+
+def rowwise_t(a_bf16_bits, offs, out=None, pow2=False):
+    return get().rowwise_t(a_bf16_bits, offs, out, pow2)
 
 
 def threads_used() -> int:

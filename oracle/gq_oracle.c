@@ -28,6 +28,10 @@
  *             round-to-nearest-even with saturation to +-448
  * The stored scale is the multiplier (448 / amax), not its reciprocal.
  *
+ * Option round_scales_to_power_of_2 (a keyword argument of the same kernel
+ * in #2668's failure report, True in that run): the scale becomes the power
+ * of two at or below it, 2^floor(log2(scale)), before the multiply.
+ *
  * Floating point: the precision is fixed to IEEE fp32 by the method, so the
  * scale and the product are computed in C `float` (FLT_EVAL_METHOD == 0 on
  * x86-64 and aarch64).  Build without -ffast-math and with
@@ -139,6 +143,19 @@ float gqo_scale(float amax) {
   return GQO_FP8_MAX / d;
 }
 
+/* 2^floor(log2(scale)) for the positive finite scales gqo_scale returns:
+ * frexp writes scale = m * 2^e with m in [0.5, 1), so floor(log2(scale)) is
+ * e - 1. */
+float gqo_scale_pow2(float amax) {
+  int e;
+  frexpf(gqo_scale(amax), &e);
+  return ldexpf(1.0f, e - 1);
+}
+
+static float gqo_scale_opt(float amax, int pow2) {
+  return pow2 ? gqo_scale_pow2(amax) : gqo_scale(amax);
+}
+
 /* q = e4m3(fp32(x * scale)). */
 uint8_t gqo_quant(uint16_t x_bf16, float scale) {
   float v = gqo_bf16_to_float(x_bf16) * scale;
@@ -168,8 +185,8 @@ static void gqo_group_bounds(const int32_t* offs, int32_t n_groups,
  * q: e4m3 codes, (M, K) row-major.  scales: fp32, (n_groups, K) row-major.
  * Returns 0, or -1 on invalid arguments.
  */
-int gqo_colwise(const uint16_t* x, int64_t M, int64_t K, const int32_t* offs,
-                int32_t n_groups, uint8_t* q, float* scales) {
+int gqo_colwise_ex(const uint16_t* x, int64_t M, int64_t K, const int32_t* offs,
+                   int32_t n_groups, int pow2, uint8_t* q, float* scales) {
   int64_t *start, *end;
   float* amax;
   int32_t g;
@@ -194,7 +211,7 @@ int gqo_colwise(const uint16_t* x, int64_t M, int64_t K, const int32_t* offs,
         float a = fabsf(gqo_bf16_to_float(x[r * K + k]));
         if (a > amax[k]) amax[k] = a;
       }
-    for (k = 0; k < K; ++k) scales[(int64_t)g * K + k] = gqo_scale(amax[k]);
+    for (k = 0; k < K; ++k) scales[(int64_t)g * K + k] = gqo_scale_opt(amax[k], pow2);
     for (r = start[g]; r < end[g]; ++r)
       for (k = 0; k < K; ++k)
         q[r * K + k] = gqo_quant(x[r * K + k], scales[(int64_t)g * K + k]);
@@ -213,9 +230,9 @@ int gqo_colwise(const uint16_t* x, int64_t M, int64_t K, const int32_t* offs,
  * transpose.  scales: fp32, (N, n_groups) row-major.
  * Returns 0, or -1 on invalid arguments.
  */
-int gqo_rowwise_t(const uint16_t* a, int64_t N, int64_t Mg,
-                  const int32_t* offs, int32_t n_groups, uint8_t* qt,
-                  float* scales) {
+int gqo_rowwise_t_ex(const uint16_t* a, int64_t N, int64_t Mg,
+                     const int32_t* offs, int32_t n_groups, int pow2, uint8_t* qt,
+                     float* scales) {
   int64_t *start, *end;
   int64_t n;
   if (N < 0 || Mg < 0 || n_groups < 1 || offs == NULL) return -1;
@@ -238,7 +255,7 @@ int gqo_rowwise_t(const uint16_t* a, int64_t N, int64_t Mg,
         float v = fabsf(gqo_bf16_to_float(a[n * Mg + m]));
         if (v > amax) amax = v;
       }
-      s = gqo_scale(amax);
+      s = gqo_scale_opt(amax, pow2);
       scales[n * n_groups + g] = s;
       for (m = start[g]; m < end[g]; ++m)
         qt[m * N + n] = gqo_quant(a[n * Mg + m], s);
@@ -247,6 +264,17 @@ int gqo_rowwise_t(const uint16_t* a, int64_t N, int64_t Mg,
   free(start);
   free(end);
   return 0;
+}
+
+/* The plain method: scales exactly 448 / max(amax, 1e-12). */
+int gqo_colwise(const uint16_t* x, int64_t M, int64_t K, const int32_t* offs,
+                int32_t n_groups, uint8_t* q, float* scales) {
+  return gqo_colwise_ex(x, M, K, offs, n_groups, 0, q, scales);
+}
+
+int gqo_rowwise_t(const uint16_t* a, int64_t N, int64_t Mg, const int32_t* offs,
+                  int32_t n_groups, uint8_t* qt, float* scales) {
+  return gqo_rowwise_t_ex(a, N, Mg, offs, n_groups, 0, qt, scales);
 }
 
 /* ----------------------------------------------- array helpers (tests) --- */
@@ -264,6 +292,11 @@ void gqo_e4m3_decode_array(const uint8_t* c, int64_t n, double* out) {
 void gqo_scale_array(const float* amax, int64_t n, float* out) {
   int64_t i;
   for (i = 0; i < n; ++i) out[i] = gqo_scale(amax[i]);
+}
+
+void gqo_scale_pow2_array(const float* amax, int64_t n, float* out) {
+  int64_t i;
+  for (i = 0; i < n; ++i) out[i] = gqo_scale_pow2(amax[i]);
 }
 
 void gqo_quant_array(const uint16_t* x, const float* scale, int64_t n,

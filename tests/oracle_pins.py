@@ -297,10 +297,52 @@ def pin_dequant_bound(o):
         assert np.all(err <= lim * (1 + 1e-6)), g
 
 
+def pin_scale_pow2(o):
+    """round_scales_to_power_of_2 (the kernel argument in #2668's failure
+    report): for every finite non-negative bf16 amax the rounded scale is an
+    exact power of two, at or below the plain scale and above half of it --
+    that is, 2^floor(log2(scale)), checked without restating the formula."""
+    bits = np.arange(0, 0x7F80, dtype=np.uint32)
+    amax = _f32_from_bits(bits << 16)
+    s = o.scale_of(amax).astype(np.float64)
+    s2 = o.scale_pow2_of(amax).astype(np.float64)
+    mant, _ = np.frexp(s2)
+    assert np.all(mant == 0.5), "not a power of two"
+    assert np.all(s2 <= s) and np.all(s < 2 * s2)
+
+
+def pin_pow2_paths(o):
+    """Both paths with power-of-two scales: every scale is the pinned
+    rounding of its amax's plain scale; each element is the e4m3 code of the
+    exact product x * 2^k (a bf16 times a power of two is exact in fp32 for
+    these magnitudes); in a group column with amax >= 1e-12 the largest code
+    lies in [224, 448]; and rowwise_t(A) == colwise(A^T) still holds."""
+    case = synth.random_case("colwise", 300, 48, 5, seed=47, n_empty=1, align=1,
+                             scale_mix=True)
+    q, s = o.colwise(case.x, case.offs, pow2=True)
+    qp, sp = o.colwise(case.x, case.offs)
+    s64, sp64 = s.astype(np.float64), sp.astype(np.float64)
+    mant, _ = np.frexp(s64)
+    assert np.all(mant == 0.5)
+    assert np.all((s64 <= sp64) & (sp64 < 2 * s64))
+    xf = ref_loop.bf16_bits_to_f32(case.x).astype(np.float64)
+    for (a, b), g in zip(ref_loop.bounds(case.offs, xf.shape[0]), range(case.n_groups)):
+        if b == a:
+            continue
+        exact = xf[a:b] * s[g].astype(np.float64)[None, :]
+        assert np.array_equal(q[a:b], o.e4m3_encode(exact.astype(np.float32))), g
+        mag = np.abs(o.e4m3_decode(q[a:b])).max(axis=0)
+        col = np.abs(xf[a:b]).max(axis=0) >= 1e-12
+        assert np.all((mag[col] >= 224) & (mag[col] <= 448)), g
+    qt, st = o.rowwise_t(np.ascontiguousarray(case.x.T), case.offs, pow2=True)
+    assert np.array_equal(qt, q) and np.array_equal(st, s.T)
+
+
 ALL_PINS = [
     pin_decode_landmarks, pin_decode_vs_torch, pin_encode_roundtrip,
     pin_encode_midpoints, pin_encode_boundaries, pin_encode_vs_torch,
     pin_scale_exact, pin_quant_single_rounding, pin_hand_examples,
     pin_paths_vs_library_loop, pin_out_of_contract_offsets,
     pin_transpose_identity, pin_max_code_invariant, pin_dequant_bound,
+    pin_scale_pow2, pin_pow2_paths,
 ]

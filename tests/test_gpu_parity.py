@@ -37,20 +37,20 @@ def dev_i32(a) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
 
 
-def run_colwise(gq, x_bits, offs, fill=SENTINEL):
+def run_colwise(gq, x_bits, offs, fill=SENTINEL, pow2=False):
     M, K = x_bits.shape
     out = torch.full((M, K), fill, dtype=torch.uint8, device="cuda")
     q, s = gq.colwise(dev_bf16(x_bits), dev_i32(offs),
-                      out=out.view(torch.float8_e4m3fn))
+                      out=out.view(torch.float8_e4m3fn), pow2_scales=pow2)
     gq.check_device_error()
     return q.view(torch.uint8).cpu().numpy(), s.cpu().numpy()
 
 
-def run_rowwise(gq, a_bits, offs, fill=SENTINEL):
+def run_rowwise(gq, a_bits, offs, fill=SENTINEL, pow2=False):
     N, Mg = a_bits.shape
     out = torch.full((Mg, N), fill, dtype=torch.uint8, device="cuda")
     q, s = gq.rowwise_t(dev_bf16(a_bits), dev_i32(offs),
-                        out=out.view(torch.float8_e4m3fn))
+                        out=out.view(torch.float8_e4m3fn), pow2_scales=pow2)
     gq.check_device_error()
     return q.view(torch.uint8).cpu().numpy(), s.cpu().numpy()
 
@@ -69,17 +69,17 @@ def assert_same(q, s, rq, rs, what):
                              f"gpu {s[i]!r} oracle {rs[i]!r}")
 
 
-def check_colwise(gq, case):
-    q, s = run_colwise(gq, case.x, case.offs)
+def check_colwise(gq, case, pow2=False):
+    q, s = run_colwise(gq, case.x, case.offs, pow2=pow2)
     fill = np.full(case.x.shape, SENTINEL, np.uint8)
-    rq, rs = oracle.colwise(case.x, case.offs, out=fill)
+    rq, rs = oracle.colwise(case.x, case.offs, out=fill, pow2=pow2)
     assert_same(q, s, rq, rs, case.name)
 
 
-def check_rowwise(gq, case):
-    q, s = run_rowwise(gq, case.x, case.offs)
+def check_rowwise(gq, case, pow2=False):
+    q, s = run_rowwise(gq, case.x, case.offs, pow2=pow2)
     fill = np.full(case.x.shape[::-1], SENTINEL, np.uint8)
-    rq, rs = oracle.rowwise_t(case.x, case.offs, out=fill)
+    rq, rs = oracle.rowwise_t(case.x, case.offs, out=fill, pow2=pow2)
     assert_same(q, s, rq, rs, case.name)
 
 
@@ -341,3 +341,38 @@ def test_host_buffer_calls(gq):
     torch.cuda.synchronize()
     rq, rs = oracle.rowwise_t(r.x, r.offs)
     assert_same(q.view(torch.uint8).numpy(), s.numpy(), rq, rs, "rowwise_t_host")
+
+
+@pytest.mark.parametrize("idx", range(4))
+def test_pow2_scales(gq, idx):
+    """round_scales_to_power_of_2 through both kernels: ragged cases with
+    empty groups, unaligned boundaries, uncovered tails and magnitudes over
+    six decades, a resident and a long rowwise unit, and empty extents."""
+    seed = 400 + idx
+    if idx == 0:
+        check_colwise(gq, synth.random_case("colwise", 777, 400, 9, seed, n_empty=2,
+                                            align=1, scale_mix=True, uncovered=7), pow2=True)
+        check_rowwise(gq, synth.random_case("rowwise_t", 144, 2000, 9, seed, n_empty=2,
+                                            align=1, scale_mix=True, uncovered=7), pow2=True)
+    elif idx == 1:
+        check_colwise(gq, synth.random_case("colwise", 4096, 256, 16, seed, n_empty=1,
+                                            scale_mix=True), pow2=True)
+        check_rowwise(gq, synth.random_case("rowwise_t", 80, 6112, 3, seed,
+                                            align=8, scale_mix=True), pow2=True)
+    elif idx == 2:  # every finite bf16 amax as a column / row maximum
+        amax = np.arange(0, 0x7F80, dtype=np.uint16)
+        rng = np.random.default_rng(seed)
+        mag = rng.integers(0, 1 << 15, size=(64, amax.size), dtype=np.uint32).astype(np.uint16)
+        x = np.minimum(mag, amax[None, :])
+        x[0] = amax
+        check_colwise(gq, synth.Case("pow2_map_c", "colwise", x, np.array([64], np.int32), 0),
+                      pow2=True)
+        check_rowwise(gq, synth.Case("pow2_map_r", "rowwise_t", np.ascontiguousarray(x.T),
+                                     np.array([64], np.int32), 0), pow2=True)
+    else:  # empty extents: only scales, all the empty group's
+        z = np.zeros((0, 32), np.uint16)
+        check_colwise(gq, synth.Case("pow2_m0", "colwise", z, np.array([0, 0], np.int32), 0),
+                      pow2=True)
+        z = np.zeros((32, 0), np.uint16)
+        check_rowwise(gq, synth.Case("pow2_mg0", "rowwise_t", z, np.array([0], np.int32), 0),
+                      pow2=True)

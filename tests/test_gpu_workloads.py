@@ -102,3 +102,28 @@ def test_rowwise_large(gq, idx, n_groups):
     gq.check_device_error()
     assert torch.equal(qt.view(torch.uint8), qc.view(torch.uint8))
     assert torch.equal(s, sc.t())
+
+
+def test_pow2_scales_full_size(gq):
+    """The two benchmark workloads with power-of-two scales, on sampled
+    columns / rows the oracle computes exactly."""
+    case = synth.workload(3, 16)
+    x, offs = dev_bf16(case.x), dev_i32(case.offs)
+    q, s = gq.colwise(x, offs, pow2_scales=True)
+    gq.check_device_error()
+    rng = np.random.default_rng(500)
+    cols = _sample(rng, case.x.shape[1], 128, 48)
+    rq, rs = oracle.colwise(case.x[:, cols], case.offs, pow2=True)
+    cols_d = torch.from_numpy(cols).cuda()
+    assert_same(q.view(torch.uint8).index_select(1, cols_d).cpu().numpy(),
+                s.index_select(1, cols_d).cpu().numpy(), rq, rs, case.name + "_pow2")
+    del x, q, s
+    case = synth.workload(5, 64)
+    a, offs = dev_bf16(case.x), dev_i32(case.offs)
+    qt, s = gq.rowwise_t(a, offs, pow2_scales=True)
+    gq.check_device_error()
+    rows = _sample(rng, case.x.shape[0], 128, 48)
+    rq, rs = oracle.rowwise_t(case.x[rows], case.offs, pow2=True)
+    rows_d = torch.from_numpy(rows).cuda()
+    assert_same(qt.view(torch.uint8).index_select(1, rows_d).cpu().numpy(),
+                s.index_select(0, rows_d).cpu().numpy(), rq, rs, case.name + "_pow2")

@@ -133,3 +133,12 @@ def test_binding_rejects_cpu_tensors(gq):
         gq.colwise(x, o)
     with pytest.raises(ValueError):
         gq.rowwise_t(x, o)
+
+
+def test_ex_calls_reject_unknown_flags(gq):
+    """The _ex calls check their flags before anything else (no GPU needed)."""
+    lib = gq.lib()
+    assert gq.GQ_SCALE_POW2 == 1
+    for bad in (2, 0x80000000, 3):
+        assert lib.gq_fp8_colwise_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1
+        assert lib.gq_fp8_rowwise_t_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1

@@ -45,6 +45,9 @@ MUTANTS = {
                                "qt[n * Mg + m] = gqo_quant(a[n * Mg + m], s);"),
     "rowwise_scale_layout": ("scales[n * n_groups + g] = s;",
                              "scales[g * N + n] = s;"),
+    "pow2_rounds_up": ("return ldexpf(1.0f, e - 1);", "return ldexpf(1.0f, e);"),
+    "pow2_ignored": ("return pow2 ? gqo_scale_pow2(amax) : gqo_scale(amax);",
+                     "return gqo_scale(amax);"),
 }
 
 
