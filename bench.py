@@ -263,6 +263,72 @@ def run_reference(args):
 
 # ------------------------------------------------------------- GPU path --
 
+EXPERT_SHAPE = (8, 4096, 4096)  # --expert-dim1: E experts of (K, N) weights
+
+
+def run_expert(args):
+    """Times the stacked expert-weight path (scales along dim1) on one GPU:
+    one call = one step; same metric and timing rules as the main bench."""
+    import numpy as np
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import fp8_quantization_moe_gb300 as gq
+    from fp8_quantization_moe_gb300 import synth
+
+    E, K, N = EXPERT_SHAPE
+    rng = np.random.default_rng(1700)
+    x = rng.standard_normal((E, K, N), dtype=np.float32)
+    x *= np.power(np.float32(10), rng.uniform(-2, 2, size=(E, 1, N))).astype(np.float32)
+    w = torch.from_numpy(synth.to_bf16_bits(x).view(np.int16)).view(torch.bfloat16).to(dev)
+    del x
+    q = torch.empty((E, K, N), dtype=torch.float8_e4m3fn, device=dev)
+    sc = torch.empty((E, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        gq.expert_dim1(w, out=q, scales=sc, stream=stream, pow2_scales=POW2)
+    torch.cuda.synchronize(dev)
+    gq.check_device_error()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        gq.expert_dim1(w, out=q, scales=sc, stream=stream, pow2_scales=POW2)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    gq.check_device_error()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    nbytes = 3 * E * K * N + 4 * E * N
+    value = nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16->e4m3 (fp32 scale math)", "data": "synthetic (seeded)",
+        "config": {"workload": f"expert weights W {E}x{K}x{N} bf16, scales along dim1 "
+                               "(per expert and column); columns scaled 10^U(-2,2)",
+                   "scales": "rounded down to powers of two" if POW2
+                             else "448 / max(amax, 1e-12)",
+                   "l2": f"input {2 * E * K * N / 2**20:.0f} MiB larger than L2; no flush"},
+        "per_call": {"us_median": statistics.median(per) * 1e3,
+                     "timing": "CUDA events on the launching stream around each C-ABI "
+                               "call (workspace clear + kernel)"},
+        "roofline": {"bound": "hbm", "kernel": "colwise (E groups of K rows)",
+                     "achieved": value, "peak": peak, "unit": "GB/s",
+                     "frac": value / peak, "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes": nbytes},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_mine(args):
     import numpy as np
     import torch
@@ -467,6 +533,9 @@ def main(argv=None):
     ap.add_argument("--pow2-scales", action="store_true",
                     help="round every scale down to a power of two (the "
                          "round_scales_to_power_of_2 option); same bytes moved")
+    ap.add_argument("--expert-dim1", action="store_true",
+                    help="time the stacked expert-weight path (8 experts of "
+                         "4096x4096, scales along dim1) instead of the main step")
     ap.add_argument("--half", action="store_true",
                     help="profiling case: half the tokens of each workload "
                          "(inputs 256 MB and 136 MB, still larger than L2); "
@@ -482,6 +551,8 @@ def main(argv=None):
         args.warmup = 3  # timing rule: at least three warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.expert_dim1:
+        return run_expert(args)
     return run_mine(args)
 
 

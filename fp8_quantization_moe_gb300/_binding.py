@@ -33,6 +33,7 @@ SIGNATURES = {
     "gq_fp8_rowwise_t": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "gq_fp8_colwise_noalloc": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P]),
     "gq_fp8_colwise_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
+    "gq_fp8_expert_dim1": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
     "gq_fp8_rowwise_t_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
     "gq_check_device_error": (ctypes.c_int, [_P]),
     "gq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -217,6 +218,35 @@ def rowwise_t(a: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
                                        _ptr(scales), GQ_SCALE_POW2 if pow2_scales else 0,
                                        wp, wn, sh)
     _check(st, "gq_fp8_rowwise_t")
+    return out, scales
+
+
+def expert_dim1(w: torch.Tensor, *, out=None, scales=None, stream=None, workspace=None,
+                pow2_scales: bool = False):
+    """Stacked expert weights scaled along dim1: w bf16 (E, K, N) CUDA tensor;
+    one scale per (expert, column), the amax over the expert's K rows.
+    Returns (q float8_e4m3fn (E, K, N), scales float32 (E, N))."""
+    if not (isinstance(w, torch.Tensor) and w.is_cuda and w.dtype == torch.bfloat16
+            and w.dim() == 3 and w.is_contiguous()):
+        raise ValueError("expert_dim1: w must be a contiguous 3-D bf16 CUDA tensor")
+    E, K, N = w.shape
+    dev = w.device
+    if out is None:
+        out = torch.empty((E, K, N), dtype=torch.float8_e4m3fn, device=dev)
+    if scales is None:
+        scales = torch.empty((E, N), dtype=torch.float32, device=dev)
+    if out.shape != (E, K, N) or out.element_size() != 1 or not out.is_contiguous():
+        raise ValueError("expert_dim1: out must be a contiguous 1-byte (E, K, N) tensor")
+    if scales.shape != (E, N) or scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError("expert_dim1: scales must be a contiguous float32 (E, N) tensor")
+    sh = _stream_handle(stream, dev)
+    need = workspace_bytes(GQ_KIND_COLWISE, E * K, N, E)
+    ws = workspace if workspace is not None else _workspace(need, dev, sh)
+    wp, wn = _ws_ptr(ws)
+    with torch.cuda.device(dev):
+        st = lib().gq_fp8_expert_dim1(_ptr(w), E, K, N, _ptr(out), _ptr(scales),
+                                      GQ_SCALE_POW2 if pow2_scales else 0, wp, wn, sh)
+    _check(st, "gq_fp8_expert_dim1")
     return out, scales
 
 

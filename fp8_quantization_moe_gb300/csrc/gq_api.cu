@@ -278,7 +278,49 @@ gq_status gq_fp8_colwise_ex(const void* x, int64_t M, int64_t K,
   if (M == 0)
     return launch_fill_empty_scales(scales, static_cast<int64_t>(n_groups) * K, flags, s);
   return colwise::launch(*info, g_dbg, x, static_cast<int32_t>(M),
-                         static_cast<int32_t>(K), offs, n_groups, out, scales,
+                         static_cast<int32_t>(K), offs, 0, n_groups, out, scales,
+                         flags, workspace, s);
+}
+
+gq_status gq_fp8_expert_dim1(const void* w, int64_t E, int64_t K, int64_t N, void* out,
+                             float* scales, uint32_t flags, void* workspace,
+                             size_t workspace_bytes, gq_stream_t stream) {
+  const char* name = "gq_fp8_expert_dim1";
+  if (flags & ~kKnownFlags)
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kKnownFlags);
+  if (E < 1 || K < 0 || N < 0)
+    return fail(GQ_ERR_INVALID_ARG, "%s: bad sizes (%lld, %lld, %lld)", name,
+                static_cast<long long>(E), static_cast<long long>(K),
+                static_cast<long long>(N));
+  if (E > GQ_MAX_GROUPS)
+    return fail(GQ_ERR_UNSUPPORTED, "%s: %lld experts > %d", name,
+                static_cast<long long>(E), GQ_MAX_GROUPS);
+  if (K > kMaxExtent || (K > 0 && E * K > kMaxExtent))  // E <= 1024: no overflow
+    return fail(GQ_ERR_UNSUPPORTED, "%s: E * K >= 2^31", name);
+  const int64_t M = E * K;
+  if (N > kMaxExtent) return fail(GQ_ERR_UNSUPPORTED, "%s: extent >= 2^31", name);
+  if (N % 16 != 0)
+    return fail(GQ_ERR_UNSUPPORTED, "%s: N = %lld is not a multiple of 16", name,
+                static_cast<long long>(N));
+  if (M > 0 && N > 0) {
+    if (w == nullptr || out == nullptr)
+      return fail(GQ_ERR_INVALID_ARG, "%s: input or output is NULL", name);
+    if (!aligned(w, 16) || !aligned(out, 16))
+      return fail(GQ_ERR_INVALID_ARG, "%s: input and output must be 16-byte aligned", name);
+  }
+  if (N > 0 && (scales == nullptr || !aligned(scales, 4)))
+    return fail(GQ_ERR_INVALID_ARG, "%s: scales NULL or misaligned", name);
+  const size_t need = gq_workspace_bytes(GQ_KIND_COLWISE, M, N, static_cast<int32_t>(E));
+  gq_status st = validate_ws(workspace, workspace_bytes, need, name);
+  if (st != GQ_OK) return st;
+  if (N == 0) return GQ_OK;
+  const DeviceInfo* info = nullptr;
+  st = current_device(&info);
+  if (st != GQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) return launch_fill_empty_scales(scales, E * N, flags, s);
+  return colwise::launch(*info, g_dbg, w, static_cast<int32_t>(M), static_cast<int32_t>(N),
+                         nullptr, static_cast<int32_t>(K), static_cast<int32_t>(E), out, scales,
                          flags, workspace, s);
 }
 

@@ -93,7 +93,8 @@ struct Smem {
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
 
 struct Params {
-  const int32_t* offs;
+  const int32_t* offs;  // nullptr: groups of `uniform` rows each
+  int32_t uniform;
   uint32_t* ticket;  // ticket counter
   uint8_t* out;
   float* scales;
@@ -119,7 +120,7 @@ __device__ __forceinline__ int stages_of(int32_t unit, int32_t M) {
 
 // ---------------------------------------------------------- context warp --
 __device__ __forceinline__ void context_warp(Smem& s, const Params& p, int lane) {
-  build_ends(p.offs, p.G, p.M, s.ends, lane);
+  build_ends(p.offs, p.uniform, p.G, p.M, s.ends, lane);
   __syncwarp();
   const int32_t units = p.sched.units;
   const uint32_t total = 2u * static_cast<uint32_t>(units) * static_cast<uint32_t>(p.sched.groups);
@@ -502,7 +503,7 @@ gq_status setup(DeviceInfo& info) {
 }
 
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
-                 int32_t M, int32_t K, const int32_t* offs, int32_t G,
+                 int32_t M, int32_t K, const int32_t* offs, int32_t uniform, int32_t G,
                  void* out, float* scales, uint32_t flags, void* ws, cudaStream_t stream) {
   CUtensorMap xmap;
   gq_status st = encode_tiled_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -524,6 +525,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   const WorkspaceLayout L = colwise_workspace(K, G);
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.offs = offs;
+  p.uniform = uniform;
   p.ticket = reinterpret_cast<uint32_t*>(w);  // first word of the header
   p.out = static_cast<uint8_t*>(out);
   p.scales = scales;

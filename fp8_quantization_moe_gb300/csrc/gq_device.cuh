@@ -389,10 +389,18 @@ __device__ __forceinline__ int32_t ld_acquire_cta_s32(const int32_t* p) {
 
 // ------------------------------------------------------ group-end table --
 // ends[g] = min(extent, max(0, offs[0..g]))  -- the running maximum clamped
-// to the extent.  Computed by one warp; `ends` is shared memory.
-__device__ __forceinline__ void build_ends(const int32_t* __restrict__ offs,
+// to the extent; with offs == nullptr, groups of `uniform` tokens each:
+// ends[g] = min(extent, (g + 1) * uniform).  Computed by one warp; `ends` is
+// shared memory.
+__device__ __forceinline__ void build_ends(const int32_t* __restrict__ offs, int32_t uniform,
                                            int n_groups, int32_t extent,
                                            int32_t* ends, int lane) {
+  if (offs == nullptr) {
+    for (int g = lane; g < n_groups; g += 32)
+      ends[g] = static_cast<int32_t>(
+          min(static_cast<int64_t>(g + 1) * uniform, static_cast<int64_t>(extent)));
+    return;
+  }
   int32_t carry = 0;
   for (int base = 0; base < n_groups; base += 32) {
     const int g = base + lane;

@@ -58,8 +58,9 @@ WorkspaceLayout colwise_workspace(int64_t K, int64_t G);
 namespace colwise {
 constexpr int kW = 128;  // columns per slab (dependency group)
 gq_status setup(DeviceInfo& info);
+// offs == nullptr: G groups of `uniform` rows each.
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
-                 int32_t M, int32_t K, const int32_t* offs, int32_t G,
+                 int32_t M, int32_t K, const int32_t* offs, int32_t uniform, int32_t G,
                  void* out, float* scales, uint32_t flags, void* ws, cudaStream_t stream);
 }  // namespace colwise
 

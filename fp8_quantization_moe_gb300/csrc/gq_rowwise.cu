@@ -152,7 +152,7 @@ __device__ __forceinline__ bool load_pass(Smem& s, const CUtensorMap* amap, uint
 // descriptors; empty groups get their scales here and no descriptor.  The
 // whole warp builds the group-end table first.
 __device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int lane) {
-  build_ends(p.offs, p.G, p.Mg, s.ends, lane);
+  build_ends(p.offs, 0, p.G, p.Mg, s.ends, lane);
   __syncwarp();
   const uint64_t wait_ns = 4 * p.timeout_ns;
   uint32_t useq = 0;  // units published

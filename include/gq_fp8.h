@@ -161,6 +161,27 @@ gq_status gq_fp8_rowwise_t_ex(const void* a, int64_t N, int64_t Mg,
                               size_t workspace_bytes, gq_stream_t stream);
 
 /*
+ * Scaling of stacked expert weights along dim1: the "fused reduction kernel
+ * along dim1 for 3d expert weights" of the pytorch/ao #2863 page's PR stack
+ * (#2865).  Each expert's (K, N) matrix is scaled per column, the amax taken
+ * over its K rows: exactly gq_fp8_colwise on the (E * K, N) stack with E
+ * token groups of K rows each, without an offsets array.
+ *
+ *   w        bf16 [E, K, N] row-major, 16-byte aligned.          (input)
+ *   E, K, N  1 <= E <= GQ_MAX_GROUPS experts; K >= 0; N >= 0, N % 16 == 0;
+ *            E * K < 2^31.
+ *   out      e4m3 bytes [E, K, N] row-major, 16-byte aligned.    (output)
+ *   scales   fp32 [E, N] row-major: scale of expert e, column n. (output)
+ *   flags    0 or GQ_SCALE_POW2.
+ *   workspace, workspace_bytes: at least gq_workspace_bytes(GQ_KIND_COLWISE,
+ *            E * K, N, E) bytes, 256-byte aligned.
+ *   stream   the CUDA stream to run on.
+ */
+gq_status gq_fp8_expert_dim1(const void* w, int64_t E, int64_t K, int64_t N, void* out,
+                             float* scales, uint32_t flags, void* workspace,
+                             size_t workspace_bytes, gq_stream_t stream);
+
+/*
  * Colwise scaling with no allocation at all, not even a caller workspace.
  * The pytorch/ao pages have no counterpart to this entry point; it exists for
  * callers that cannot obtain device memory at the point where they quantize

@@ -64,6 +64,8 @@ class Oracle:
         lib.gqo_colwise_ex.restype = ctypes.c_int
         lib.gqo_rowwise_t_ex.argtypes = [p, i64, i64, p, i32, ctypes.c_int, p, p]
         lib.gqo_rowwise_t_ex.restype = ctypes.c_int
+        lib.gqo_expert_dim1.argtypes = [p, i64, i64, i64, ctypes.c_int, p, p]
+        lib.gqo_expert_dim1.restype = ctypes.c_int
         lib.gqo_scale_pow2_array.argtypes = [p, i64, p]
         lib.gqo_scale_pow2_array.restype = None
         lib.gqo_e4m3_encode_array.argtypes = [p, i64, p]
@@ -158,6 +160,22 @@ class Oracle:
         return qt, s
 
 
+    def expert_dim1(self, w_bf16_bits, pow2=False):
+        """Stacked expert weights (E, K, N) scaled per (expert, column), the
+        amax over each expert's K rows.  Returns (q uint8 (E, K, N), scales
+        float32 (E, N))."""
+        w = _c(w_bf16_bits, np.uint16)
+        assert w.ndim == 3
+        E, K, N = w.shape
+        q = np.zeros((E, K, N), np.uint8)
+        s = np.empty((E, N), np.float32)
+        rc = self.lib.gqo_expert_dim1(w.ctypes.data, E, K, N, int(bool(pow2)),
+                                      q.ctypes.data, s.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle expert_dim1: invalid arguments")
+        return q, s
+
+
 _lock = threading.Lock()
 _default: Oracle | None = None
 
@@ -197,6 +215,10 @@ def colwise(x_bf16_bits, offs, out=None, pow2=False):
 
 def rowwise_t(a_bf16_bits, offs, out=None, pow2=False):
     return get().rowwise_t(a_bf16_bits, offs, out, pow2)
+
+
+def expert_dim1(w_bf16_bits, pow2=False):
+    return get().expert_dim1(w_bf16_bits, pow2)
 
 
 def threads_used() -> int:

@@ -266,6 +266,36 @@ int gqo_rowwise_t_ex(const uint16_t* a, int64_t N, int64_t Mg,
   return 0;
 }
 
+/* -------------------------------------------------- expert weights --- */
+
+/*
+ * Stacked expert weights w: bf16 bits, (E, K, N) row-major.  For each expert
+ * e and column n the amax is taken over the K rows of that expert (a
+ * reduction along dim1, the "fused reduction kernel along dim1 for 3d expert
+ * weights" of the #2863 page's PR stack); q has w's layout, scales are
+ * (E, N) row-major.  Returns 0, or -1 on invalid arguments.
+ */
+int gqo_expert_dim1(const uint16_t* w, int64_t E, int64_t K, int64_t N, int pow2,
+                    uint8_t* q, float* scales) {
+  int64_t e, k, n;
+  if (E < 1 || K < 0 || N < 0) return -1;
+  if ((E * K * N > 0) && (w == NULL || q == NULL)) return -1;
+  if (N > 0 && scales == NULL) return -1;
+  for (e = 0; e < E; ++e)
+    for (n = 0; n < N; ++n) {
+      float amax = 0.0f, s;
+      for (k = 0; k < K; ++k) {
+        float a = fabsf(gqo_bf16_to_float(w[(e * K + k) * N + n]));
+        if (a > amax) amax = a;
+      }
+      s = gqo_scale_opt(amax, pow2);
+      scales[e * N + n] = s;
+      for (k = 0; k < K; ++k)
+        q[(e * K + k) * N + n] = gqo_quant(w[(e * K + k) * N + n], s);
+    }
+  return 0;
+}
+
 /* The plain method: scales exactly 448 / max(amax, 1e-12). */
 int gqo_colwise(const uint16_t* x, int64_t M, int64_t K, const int32_t* offs,
                 int32_t n_groups, uint8_t* q, float* scales) {

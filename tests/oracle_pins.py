@@ -338,11 +338,38 @@ def pin_pow2_paths(o):
     assert np.array_equal(qt, q) and np.array_equal(st, s.T)
 
 
+def pin_expert_dim1(o):
+    """Stacked expert weights along dim1: a numpy / torch restatement of the
+    definition (per expert and column: amax over the expert's K rows, fp32
+    scale, torch's RNE-saturating e4m3 cast of the fp32 product) on ragged
+    small shapes with per-row magnitudes over six decades, K = 0 included;
+    and the identity with colwise on the (E * K, N) stack with E groups of
+    K rows."""
+    rng = np.random.default_rng(49)
+    for E, K, N in ((1, 5, 16), (3, 50, 32), (4, 0, 16), (2, 33, 48)):
+        x = rng.standard_normal((E, K, N)).astype(np.float32)
+        x *= np.power(np.float32(10), rng.uniform(-3, 3, size=(E, K, 1))).astype(np.float32)
+        w = synth.to_bf16_bits(x)
+        q, s = o.expert_dim1(w)
+        wf = ref_loop.bf16_bits_to_f32(w)
+        for e in range(E):
+            amax = np.abs(wf[e]).max(axis=0) if K else np.zeros(N, np.float32)
+            se = np.float32(448.0) / np.maximum(amax, np.float32(1e-12))
+            assert np.array_equal(s[e], se.astype(np.float32)), (E, K, N, e)
+            if K:
+                v = (wf[e] * se[None, :]).astype(np.float32)
+                assert np.array_equal(q[e], _torch_e4m3(np.clip(v, -448, 448))), (E, K, N, e)
+        if K:
+            offs = (np.arange(1, E + 1) * K).astype(np.int32)
+            qc, sc = o.colwise(w.reshape(E * K, N), offs)
+            assert np.array_equal(qc, q.reshape(E * K, N)) and np.array_equal(sc, s)
+
+
 ALL_PINS = [
     pin_decode_landmarks, pin_decode_vs_torch, pin_encode_roundtrip,
     pin_encode_midpoints, pin_encode_boundaries, pin_encode_vs_torch,
     pin_scale_exact, pin_quant_single_rounding, pin_hand_examples,
     pin_paths_vs_library_loop, pin_out_of_contract_offsets,
     pin_transpose_identity, pin_max_code_invariant, pin_dequant_bound,
-    pin_scale_pow2, pin_pow2_paths,
+    pin_scale_pow2, pin_pow2_paths, pin_expert_dim1,
 ]

@@ -376,3 +376,24 @@ def test_pow2_scales(gq, idx):
         z = np.zeros((32, 0), np.uint16)
         check_rowwise(gq, synth.Case("pow2_mg0", "rowwise_t", z, np.array([0], np.int32), 0),
                       pow2=True)
+
+
+@pytest.mark.parametrize("E,K,N,pow2", [
+    (1, 64, 16, False), (3, 100, 48, False), (8, 333, 272, False), (5, 257, 4112, True),
+    (2, 1, 16, False), (5, 0, 32, False), (4, 17, 0, False), (64, 40, 32, True),
+])
+def test_expert_dim1(gq, E, K, N, pow2):
+    """Stacked expert weights scaled along dim1, against the oracle, bit for
+    bit: ragged K and N over several tiles, one-row experts, K = 0 (scales
+    only), N = 0 (nothing), many experts."""
+    rng = np.random.default_rng(600 + E + K + N)
+    x = rng.standard_normal((E, K, N)).astype(np.float32)
+    x *= np.power(np.float32(10), rng.uniform(-3, 3, size=(E, K, 1))).astype(np.float32)
+    w = synth.to_bf16_bits(x)
+    out = torch.full((E, K, N), SENTINEL, dtype=torch.uint8, device="cuda")
+    wd = torch.from_numpy(np.ascontiguousarray(w).view(np.int16)).view(torch.bfloat16).cuda()
+    q, s = gq.expert_dim1(wd, out=out.view(torch.float8_e4m3fn), pow2_scales=pow2)
+    gq.check_device_error()
+    rq, rs = oracle.expert_dim1(w, pow2=pow2)
+    assert_same(q.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), rq, rs,
+                f"expert_dim1_{E}x{K}x{N}")

@@ -127,3 +127,22 @@ def test_pow2_scales_full_size(gq):
     rows_d = torch.from_numpy(rows).cuda()
     assert_same(qt.view(torch.uint8).index_select(1, rows_d).cpu().numpy(),
                 s.index_select(0, rows_d).cpu().numpy(), rq, rs, case.name + "_pow2")
+
+
+def test_expert_dim1_full_size(gq):
+    """Eight experts of (4096, 4096) bf16 weights -- 256 MB, larger than L2 --
+    on sampled columns, which the oracle computes exactly."""
+    rng = np.random.default_rng(601)
+    E, K, N = 8, 4096, 4096
+    x = rng.standard_normal((E, K, N), dtype=np.float32)
+    x *= np.power(np.float32(10), rng.uniform(-2, 2, size=(E, 1, N))).astype(np.float32)
+    w = synth.to_bf16_bits(x)
+    del x
+    wd = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).cuda()
+    q, s = gq.expert_dim1(wd)
+    gq.check_device_error()
+    cols = _sample(rng, N, 128, 48)
+    rq, rs = oracle.expert_dim1(np.ascontiguousarray(w[:, :, cols]))
+    cols_d = torch.from_numpy(cols).cuda()
+    assert_same(q.view(torch.uint8).index_select(2, cols_d).cpu().numpy(),
+                s.index_select(1, cols_d).cpu().numpy(), rq, rs, "expert_dim1_8x4096x4096")

@@ -142,3 +142,18 @@ def test_ex_calls_reject_unknown_flags(gq):
     for bad in (2, 0x80000000, 3):
         assert lib.gq_fp8_colwise_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1
         assert lib.gq_fp8_rowwise_t_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1
+
+
+@pytest.mark.parametrize("args,status", [
+    # w, E, K, N, out, scales, flags, ws, ws_bytes
+    ((A16, 0, 16, 16, A16, A16, 0, A16, 1 << 20), 1),      # no experts
+    ((A16, 2000, 16, 16, A16, A16, 0, A16, 1 << 20), 2),   # > GQ_MAX_GROUPS
+    ((A16, 2, 16, 24, A16, A16, 0, A16, 1 << 20), 2),      # N % 16
+    ((A16, 2, -1, 16, A16, A16, 0, A16, 1 << 20), 1),      # negative K
+    ((A16, 2, 16, 16, A16, A16, 4, A16, 1 << 20), 1),      # unknown flag
+    ((A16, 2, 16, 16, None, A16, 0, A16, 1 << 20), 1),     # NULL output
+    ((A16, 2, 16, 16, A16, A16, 0, A16, 100), 1),          # workspace too small
+    ((A16, 4, 1 << 30, 16, A16, A16, 0, A16, 1 << 20), 2),  # E * K >= 2^31
+])
+def test_expert_dim1_host_validation(gq, args, status):
+    assert gq.lib().gq_fp8_expert_dim1(*args, None) == status

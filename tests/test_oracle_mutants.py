@@ -46,6 +46,8 @@ MUTANTS = {
     "rowwise_scale_layout": ("scales[n * n_groups + g] = s;",
                              "scales[g * N + n] = s;"),
     "pow2_rounds_up": ("return ldexpf(1.0f, e - 1);", "return ldexpf(1.0f, e);"),
+    "expert_amax_ignores_expert": ("float a = fabsf(gqo_bf16_to_float(w[(e * K + k) * N + n]));",
+                                   "float a = fabsf(gqo_bf16_to_float(w[k * N + n]));"),
     "pow2_ignored": ("return pow2 ? gqo_scale_pow2(amax) : gqo_scale(amax);",
                      "return gqo_scale(amax);"),
 }
