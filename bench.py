@@ -329,6 +329,61 @@ def run_expert(args):
     return 0
 
 
+def run_mxfp8(args):
+    """Times the mxfp8 dim0 cast on the colwise benchmark input X (65536,
+    4096): one call = one step."""
+    import numpy as np
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import fp8_quantization_moe_gb300 as gq
+    from fp8_quantization_moe_gb300 import synth
+
+    M, K, G = COLWISE_SHAPE
+    c = synth.colwise_large(G, rows=M, cols=K)
+    x = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).to(dev)
+    q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    sc = torch.empty((M, K // 32), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        gq.mxfp8_dim0(x, args.mxfp8, out=q, scales=sc, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        gq.mxfp8_dim0(x, args.mxfp8, out=q, scales=sc, stream=stream)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    nbytes = 3 * M * K + M * K // 32
+    value = nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16->e4m3 + e8m0 block scales", "data": "synthetic (seeded)",
+        "config": {"workload": f"mxfp8 dim0 cast ({args.mxfp8.upper()}) of X {M}x{K} bf16, "
+                               "32-element row blocks; rows scaled 10^U(-2,2)",
+                   "l2": f"input {2 * M * K / 2**20:.0f} MiB larger than L2; no flush"},
+        "per_call": {"us_median": statistics.median(per) * 1e3,
+                     "timing": "CUDA events on the launching stream around each call"},
+        "roofline": {"bound": "hbm", "kernel": "mx_kernel", "achieved": value, "peak": peak,
+                     "unit": "GB/s", "frac": value / peak, "peak_kind": peak_kind,
+                     "traffic": None,
+                     "algorithmic_bytes": nbytes},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_mine(args):
     import numpy as np
     import torch
@@ -536,6 +591,9 @@ def main(argv=None):
     ap.add_argument("--expert-dim1", action="store_true",
                     help="time the stacked expert-weight path (8 experts of "
                          "4096x4096, scales along dim1) instead of the main step")
+    ap.add_argument("--mxfp8", choices=["floor", "rceil"], default=None,
+                    help="time the mxfp8 dim0 cast of the colwise input instead "
+                         "of the main step")
     ap.add_argument("--half", action="store_true",
                     help="profiling case: half the tokens of each workload "
                          "(inputs 256 MB and 136 MB, still larger than L2); "
@@ -553,6 +611,8 @@ def main(argv=None):
         return run_reference(args)
     if args.expert_dim1:
         return run_expert(args)
+    if args.mxfp8:
+        return run_mxfp8(args)
     return run_mine(args)
 
 

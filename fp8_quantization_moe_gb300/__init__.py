@@ -7,7 +7,9 @@ Two paths, both in hand-written sm_103a CUDA kernels behind the C ABI of
 * ``rowwise_t(a, offs)`` -- groups along dim1: one scale per (row, group), fp8
   output written transposed;
 * ``expert_dim1(w)``     -- stacked expert weights (E, K, N): one scale per
-  (expert, column), reduced along dim1.
+  (expert, column), reduced along dim1;
+* ``mxfp8_dim0(x, mode)`` -- mxfp8: 32-element row blocks with e8m0 scales
+  (FLOOR or RCEIL).
 
 scale = 448 / max(amax, 1e-12) in IEEE fp32; q = saturating round-to-nearest-
 even e4m3 cast of fp32(x * scale); ``pow2_scales=True`` rounds every scale
@@ -17,7 +19,7 @@ supplies device memory and streams.  ``synth`` draws seeded inputs.
 """
 from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
                        GQ_SCALE_POW2, GQError, check_device_error, colwise, colwise_host,
-                       colwise_noalloc, expert_dim1,
+                       colwise_noalloc, expert_dim1, mxfp8_dim0,
                        debug_set, lib, library_path, rowwise_t,
                        rowwise_t_host, set_lag, status_string, version,
                        workspace_bytes)
@@ -26,7 +28,7 @@ from ._build import build
 __all__ = [
     "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQ_SCALE_POW2", "GQError",
     "build", "check_device_error", "colwise", "colwise_host",
-    "colwise_noalloc", "debug_set", "expert_dim1",
+    "colwise_noalloc", "debug_set", "expert_dim1", "mxfp8_dim0",
     "lib", "library_path", "rowwise_t", "rowwise_t_host", "set_lag",
     "status_string",
     "version", "workspace_bytes",

@@ -24,6 +24,8 @@ GQ_KIND_COLWISE = 0
 GQ_KIND_ROWWISE_T = 1
 GQ_MAX_GROUPS = 1024
 GQ_SCALE_POW2 = 1
+GQ_MX_FLOOR = 0
+GQ_MX_RCEIL = 1
 
 # Every symbol the header declares, with its ctypes signature.
 _P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
@@ -34,6 +36,7 @@ SIGNATURES = {
     "gq_fp8_colwise_noalloc": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P]),
     "gq_fp8_colwise_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
     "gq_fp8_expert_dim1": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
+    "gq_mxfp8_dim0": (ctypes.c_int, [_P, _I64, _I64, _P, _P, ctypes.c_int, _P]),
     "gq_fp8_rowwise_t_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
     "gq_check_device_error": (ctypes.c_int, [_P]),
     "gq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -247,6 +250,34 @@ def expert_dim1(w: torch.Tensor, *, out=None, scales=None, stream=None, workspac
         st = lib().gq_fp8_expert_dim1(_ptr(w), E, K, N, _ptr(out), _ptr(scales),
                                       GQ_SCALE_POW2 if pow2_scales else 0, wp, wn, sh)
     _check(st, "gq_fp8_expert_dim1")
+    return out, scales
+
+
+def mxfp8_dim0(x: torch.Tensor, mode: str = "floor", *, out=None, scales=None, stream=None):
+    """mxfp8 cast along dim0: blocks of 32 consecutive elements of a row share
+    a power-of-two scale.  x bf16 (M, K) CUDA tensor, K % 32 == 0; mode
+    "floor" or "rceil".  Returns (q float8_e4m3fn (M, K), scales uint8
+    (M, K // 32) e8m0 bytes)."""
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.bfloat16
+            and x.dim() == 2 and x.is_contiguous()):
+        raise ValueError("mxfp8_dim0: x must be a contiguous 2-D bf16 CUDA tensor")
+    modes = {"floor": GQ_MX_FLOOR, "rceil": GQ_MX_RCEIL}
+    if mode not in modes:
+        raise ValueError("mxfp8_dim0: mode must be 'floor' or 'rceil'")
+    M, K = x.shape
+    dev = x.device
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    if scales is None:
+        scales = torch.empty((M, K // 32), dtype=torch.uint8, device=dev)
+    if out.shape != (M, K) or out.element_size() != 1 or not out.is_contiguous():
+        raise ValueError("mxfp8_dim0: out must be a contiguous 1-byte (M, K) tensor")
+    if scales.shape != (M, K // 32) or scales.element_size() != 1 or not scales.is_contiguous():
+        raise ValueError("mxfp8_dim0: scales must be a contiguous 1-byte (M, K // 32) tensor")
+    sh = _stream_handle(stream, dev)
+    with torch.cuda.device(dev):
+        st = lib().gq_mxfp8_dim0(_ptr(x), M, K, _ptr(out), _ptr(scales), modes[mode], sh)
+    _check(st, "gq_mxfp8_dim0")
     return out, scales
 
 

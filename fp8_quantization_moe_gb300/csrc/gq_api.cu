@@ -74,6 +74,8 @@ void setup_device(int dev) {
   st = colwise::setup(info);
   if (st != GQ_OK) return;
   st = rowwise::setup(info);
+  if (st != GQ_OK) return;
+  st = mx::setup(info);
 }
 
 // Set-up for the current device (once per device per process).
@@ -362,6 +364,30 @@ gq_status gq_fp8_rowwise_t_ex(const void* a, int64_t N, int64_t Mg,
   return rowwise::launch(*info, g_dbg, a, static_cast<int32_t>(N),
                          static_cast<int32_t>(Mg), offs, n_groups, out_t, scales,
                          flags, workspace, s);
+}
+
+gq_status gq_mxfp8_dim0(const void* x, int64_t M, int64_t K, void* out, uint8_t* scales,
+                        int mode, gq_stream_t stream) {
+  const char* name = "gq_mxfp8_dim0";
+  if (mode != GQ_MX_FLOOR && mode != GQ_MX_RCEIL)
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown mode %d", name, mode);
+  if (M < 0 || K < 0)
+    return fail(GQ_ERR_INVALID_ARG, "%s: negative size (%lld, %lld)", name,
+                static_cast<long long>(M), static_cast<long long>(K));
+  if (M > kMaxExtent || K > kMaxExtent)
+    return fail(GQ_ERR_UNSUPPORTED, "%s: extent >= 2^31", name);
+  if (K % 32 != 0)
+    return fail(GQ_ERR_UNSUPPORTED, "%s: K = %lld is not a multiple of 32", name,
+                static_cast<long long>(K));
+  if (M == 0 || K == 0) return GQ_OK;
+  if (x == nullptr || out == nullptr || scales == nullptr)
+    return fail(GQ_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  if (!aligned(x, 16) || !aligned(out, 16))
+    return fail(GQ_ERR_INVALID_ARG, "%s: input and output must be 16-byte aligned", name);
+  const DeviceInfo* info = nullptr;
+  gq_status st = current_device(&info);
+  if (st != GQ_OK) return st;
+  return mx::launch(*info, x, M, K, out, scales, mode, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gq_status gq_check_device_error(gq_stream_t stream) {

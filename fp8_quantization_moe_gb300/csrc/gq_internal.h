@@ -18,6 +18,7 @@ struct DeviceInfo {
   unsigned* err_word = nullptr;  // device address of the error word
   int colwise_ctas_per_sm = 0;
   int rowwise_ctas_per_sm = 0;
+  int mx_ctas_per_sm = 0;
 };
 
 // Launch-time knobs (test hooks).
@@ -73,6 +74,12 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
                  int32_t N, int32_t Mg, const int32_t* offs, int32_t G,
                  void* out_t, float* scales, uint32_t flags, void* ws, cudaStream_t stream);
 }  // namespace rowwise
+
+namespace mx {
+gq_status setup(DeviceInfo& info);
+gq_status launch(const DeviceInfo& info, const void* x, int64_t M, int64_t K, void* out,
+                 uint8_t* scales, int mode, cudaStream_t stream);
+}  // namespace mx
 
 // Writes the scale of an empty group -- 448 / 1e-12 (fp32), or its power
 // of two below with GQ_SCALE_POW2 -- into n scales: every group is empty

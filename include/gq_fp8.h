@@ -182,6 +182,28 @@ gq_status gq_fp8_expert_dim1(const void* w, int64_t E, int64_t K, int64_t N, voi
                              size_t workspace_bytes, gq_stream_t stream);
 
 /*
+ * mxfp8 cast along dim0 (pytorch/ao page "[mxfp8 moe training] fix mxfp8
+ * a2a bench script; set mxfp8 a2a scaling type to RCEIL", Summary: the
+ * dim0_mxfp8_floor cast benchmark and the RCEIL scaling type).  Every 32
+ * consecutive elements of a row form a block sharing one power-of-two scale
+ * 2^E, stored as the e8m0 byte E + 127; q = e4m3(fp32(x * 2^-E)), saturating
+ * round-to-nearest-even.
+ *   mode GQ_MX_FLOOR:  E = floor(log2(amax)) - 8 (the exponent of 448);
+ *   mode GQ_MX_RCEIL:  E = ceil(log2(fp32(amax / 448))).
+ * E is clamped to [-127, 127]; a block with amax 0 gets E = -127 (byte 0).
+ *
+ *   x        bf16 [M, K] row-major, 16-byte aligned.             (input)
+ *   M, K     M >= 0, K >= 0, K % 32 == 0.
+ *   out      e4m3 bytes [M, K] row-major, 16-byte aligned.       (output)
+ *   scales   e8m0 bytes [M, K / 32] row-major.                   (output)
+ *   stream   the CUDA stream to run on.  No workspace.
+ */
+#define GQ_MX_FLOOR 0
+#define GQ_MX_RCEIL 1
+gq_status gq_mxfp8_dim0(const void* x, int64_t M, int64_t K, void* out, uint8_t* scales,
+                        int mode, gq_stream_t stream);
+
+/*
  * Colwise scaling with no allocation at all, not even a caller workspace.
  * The pytorch/ao pages have no counterpart to this entry point; it exists for
  * callers that cannot obtain device memory at the point where they quantize

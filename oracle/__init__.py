@@ -64,6 +64,8 @@ class Oracle:
         lib.gqo_colwise_ex.restype = ctypes.c_int
         lib.gqo_rowwise_t_ex.argtypes = [p, i64, i64, p, i32, ctypes.c_int, p, p]
         lib.gqo_rowwise_t_ex.restype = ctypes.c_int
+        lib.gqo_mxfp8_dim0.argtypes = [p, i64, i64, ctypes.c_int, p, p]
+        lib.gqo_mxfp8_dim0.restype = ctypes.c_int
         lib.gqo_expert_dim1.argtypes = [p, i64, i64, i64, ctypes.c_int, p, p]
         lib.gqo_expert_dim1.restype = ctypes.c_int
         lib.gqo_scale_pow2_array.argtypes = [p, i64, p]
@@ -176,6 +178,22 @@ class Oracle:
         return q, s
 
 
+    def mxfp8_dim0(self, x_bf16_bits, mode):
+        """mxfp8 cast along dim0: blocks of 32 consecutive elements of a row
+        share a power-of-two scale.  mode 0 = FLOOR, 1 = RCEIL.  Returns
+        (q uint8 (M, K) e4m3 codes, scales uint8 (M, K / 32) e8m0 bytes)."""
+        x = _c(x_bf16_bits, np.uint16)
+        assert x.ndim == 2
+        M, K = x.shape
+        q = np.zeros((M, K), np.uint8)
+        s = np.zeros((M, K // 32), np.uint8)
+        rc = self.lib.gqo_mxfp8_dim0(x.ctypes.data, M, K, int(mode), q.ctypes.data,
+                                     s.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle mxfp8_dim0: invalid arguments")
+        return q, s
+
+
 _lock = threading.Lock()
 _default: Oracle | None = None
 
@@ -219,6 +237,10 @@ def rowwise_t(a_bf16_bits, offs, out=None, pow2=False):
 
 def expert_dim1(w_bf16_bits, pow2=False):
     return get().expert_dim1(w_bf16_bits, pow2)
+
+
+def mxfp8_dim0(x_bf16_bits, mode):
+    return get().mxfp8_dim0(x_bf16_bits, mode)
 
 
 def threads_used() -> int:

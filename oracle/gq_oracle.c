@@ -296,6 +296,64 @@ int gqo_expert_dim1(const uint16_t* w, int64_t E, int64_t K, int64_t N, int pow2
   return 0;
 }
 
+/* ------------------------------------------------------ mxfp8 dim0 --- */
+
+/*
+ * mxfp8 cast along dim0 (the "dim0_mxfp8_floor" cast benchmark and the RCEIL
+ * scaling type of the pytorch/ao "fix mxfp8 a2a bench script; set mxfp8 a2a
+ * scaling type to RCEIL" page): every 32 consecutive elements of a row form
+ * a block that shares one power-of-two scale 2^E, stored as an e8m0 byte
+ * E + 127; elements are e4m3(fp32(x * 2^-E)).
+ *   FLOOR (mode 0): E = floor(log2(amax)) - 8, 8 being the exponent of
+ *                   e4m3's largest value (448 = 1.75 * 2^8);
+ *   RCEIL (mode 1): E = ceil(log2(v)), v = fp32(amax / 448), the power of
+ *                   two at or above the block's amax over 448.
+ * E is clamped to [-127, 127]; a block whose amax is 0 gets E = -127 (byte
+ * 0) and all-zero elements.
+ */
+static int gqo_mx_exponent(float amax, int mode) {
+  int e, E;
+  float v;
+  if (amax == 0.0f) return -127;
+  if (mode == 0) {
+    frexpf(amax, &e);  /* amax = m * 2^e, m in [0.5, 1): floor(log2) = e - 1 */
+    E = (e - 1) - 8;
+  } else {
+    v = amax / GQO_FP8_MAX;
+    /* v = m * 2^e with m in [0.5, 1): ceil(log2 v) is e - 1 when m == 0.5
+     * (v a power of two), else e */
+    E = (frexpf(v, &e) == 0.5f) ? e - 1 : e;
+  }
+  if (E < -127) E = -127;
+  if (E > 127) E = 127;
+  return E;
+}
+
+/* x: bf16 bits (M, K) row-major, K % 32 == 0.  q: e4m3 (M, K); scales:
+ * e8m0 bytes (M, K / 32).  Returns 0, or -1 on invalid arguments. */
+int gqo_mxfp8_dim0(const uint16_t* x, int64_t M, int64_t K, int mode, uint8_t* q,
+                   uint8_t* scales) {
+  int64_t r, b, i, nb;
+  if (M < 0 || K < 0 || K % 32 != 0 || (mode != 0 && mode != 1)) return -1;
+  if (M * K > 0 && (x == NULL || q == NULL || scales == NULL)) return -1;
+  nb = K / 32;
+  for (r = 0; r < M; ++r)
+    for (b = 0; b < nb; ++b) {
+      const uint16_t* xb = x + r * K + b * 32;
+      float amax = 0.0f, f;
+      int E;
+      for (i = 0; i < 32; ++i) {
+        float a = fabsf(gqo_bf16_to_float(xb[i]));
+        if (a > amax) amax = a;
+      }
+      E = gqo_mx_exponent(amax, mode);
+      scales[r * nb + b] = (uint8_t)(E + 127);
+      f = ldexpf(1.0f, -E);
+      for (i = 0; i < 32; ++i) q[r * K + b * 32 + i] = gqo_e4m3_encode(gqo_bf16_to_float(xb[i]) * f);
+    }
+  return 0;
+}
+
 /* The plain method: scales exactly 448 / max(amax, 1e-12). */
 int gqo_colwise(const uint16_t* x, int64_t M, int64_t K, const int32_t* offs,
                 int32_t n_groups, uint8_t* q, float* scales) {

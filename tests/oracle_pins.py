@@ -365,11 +365,64 @@ def pin_expert_dim1(o):
             assert np.array_equal(qc, q.reshape(E * K, N)) and np.array_equal(sc, s)
 
 
+def _mx_input(rng, M, K):
+    """Rows of blocks with magnitudes from 2^-140 to 2^120, zero blocks,
+    bf16 subnormals, signed zeros and exact powers of two."""
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x *= np.power(np.float32(2), rng.integers(-140, 121, size=(M, K // 32, 1)).astype(np.float32)
+                  ).repeat(32, axis=2).reshape(M, K)
+    bits = synth.to_bf16_bits(x)
+    special = [
+        np.zeros(32, np.uint16),                                      # a zero block
+        np.full(32, 0x8000, np.uint16),                               # negative zeros
+        np.arange(1, 33, dtype=np.uint16),                            # bf16 subnormals
+        0x4000 | np.arange(0, 32, dtype=np.uint16) % 2 * 0x0080,      # 2 and 4
+    ]
+    per_row = 2 if K >= 64 else 1          # two special blocks a row where they fit
+    for i, blk in enumerate(special):
+        r, c = divmod(i, per_row)
+        if r < M:
+            bits[r, 32 * c:32 * c + 32] = blk
+    return bits
+
+
+def pin_mxfp8_dim0(o):
+    """mxfp8 along dim0, checked block by block without restating the
+    exponent rule: zero blocks get byte 0 and zero codes; otherwise, with
+    E = byte - 127 and E not clamped, amax * 2^-E lies in [256, 512) under
+    FLOOR and in (224, 448] under RCEIL (up to the rounding of amax / 448),
+    and every element is torch's saturating RNE e4m3 cast of the fp32
+    product x * 2^-E."""
+    rng = np.random.default_rng(53)
+    bits = _mx_input(rng, 24, 256)
+    xf = ref_loop.bf16_bits_to_f32(bits)
+    for mode in (0, 1):
+        q, s = o.mxfp8_dim0(bits, mode)
+        E = s.astype(np.int64) - 127
+        for r in range(bits.shape[0]):
+            for b in range(bits.shape[1] // 32):
+                xb = xf[r, 32 * b:32 * b + 32]
+                amax = float(np.abs(xb).max())
+                if amax == 0.0:
+                    assert s[r, b] == 0 and not np.any(q[r, 32 * b:32 * b + 32] & 0x7F)
+                    continue
+                e = int(E[r, b])
+                t = amax * 2.0 ** -e
+                if -127 < e < 127:
+                    if mode == 0:
+                        assert 256 <= t < 512, (r, b, amax, e)
+                    else:
+                        assert 224 * (1 - 2 ** -23) < t <= 448 * (1 + 2 ** -23), (r, b, amax, e)
+                f = np.float32(np.ldexp(1.0, -e))
+                want = _torch_e4m3(np.clip((xb * f).astype(np.float32), -448, 448))
+                assert np.array_equal(q[r, 32 * b:32 * b + 32], want), (mode, r, b)
+
+
 ALL_PINS = [
     pin_decode_landmarks, pin_decode_vs_torch, pin_encode_roundtrip,
     pin_encode_midpoints, pin_encode_boundaries, pin_encode_vs_torch,
     pin_scale_exact, pin_quant_single_rounding, pin_hand_examples,
     pin_paths_vs_library_loop, pin_out_of_contract_offsets,
     pin_transpose_identity, pin_max_code_invariant, pin_dequant_bound,
-    pin_scale_pow2, pin_pow2_paths, pin_expert_dim1,
+    pin_scale_pow2, pin_pow2_paths, pin_expert_dim1, pin_mxfp8_dim0,
 ]

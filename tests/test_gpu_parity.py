@@ -397,3 +397,24 @@ def test_expert_dim1(gq, E, K, N, pow2):
     rq, rs = oracle.expert_dim1(w, pow2=pow2)
     assert_same(q.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), rq, rs,
                 f"expert_dim1_{E}x{K}x{N}")
+
+
+@pytest.mark.parametrize("M,K,mode", [
+    (1, 32, "floor"), (1, 32, "rceil"), (24, 256, "floor"), (24, 256, "rceil"),
+    (333, 4096, "floor"), (333, 4096, "rceil"), (4097, 96, "rceil"), (0, 64, "floor"),
+])
+def test_mxfp8_dim0(gq, M, K, mode):
+    """mxfp8 along dim0 against the oracle, bit for bit (codes and e8m0
+    bytes): block magnitudes from 2^-140 to 2^120 (clamped exponents at both
+    ends), zero and negative-zero blocks, bf16 subnormals, exact powers of
+    two, ragged M and a chunk count that is not a multiple of the grid's."""
+    import oracle_pins
+    rng = np.random.default_rng(700 + M + K)
+    bits = oracle_pins._mx_input(rng, M, K)
+    x = dev_bf16(bits) if M else torch.empty((0, K), dtype=torch.bfloat16, device="cuda")
+    q, s = gq.mxfp8_dim0(x, mode)
+    torch.cuda.synchronize()
+    rq, rs = oracle.mxfp8_dim0(bits, 0 if mode == "floor" else 1)
+    gq_q, gq_s = q.view(torch.uint8).cpu().numpy(), s.cpu().numpy()
+    assert np.array_equal(gq_s, rs), f"{mode} scales: {np.argwhere(gq_s != rs)[:3]}"
+    assert np.array_equal(gq_q, rq), f"{mode} codes: {np.argwhere(gq_q != rq)[:3]}"

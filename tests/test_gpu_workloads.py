@@ -146,3 +146,18 @@ def test_expert_dim1_full_size(gq):
     cols_d = torch.from_numpy(cols).cuda()
     assert_same(q.view(torch.uint8).index_select(2, cols_d).cpu().numpy(),
                 s.index_select(1, cols_d).cpu().numpy(), rq, rs, "expert_dim1_8x4096x4096")
+
+
+@pytest.mark.parametrize("mode", ["floor", "rceil"])
+def test_mxfp8_full_size(gq, mode):
+    """The colwise benchmark input X (65536, 4096) through the mxfp8 cast, on
+    sampled rows (the cast is row-local, so the oracle computes them exactly)."""
+    case = synth.workload(3, 16)
+    q, s = gq.mxfp8_dim0(dev_bf16(case.x), mode)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(701)
+    rows = _sample(rng, case.x.shape[0], 64, 64)
+    rq, rs = oracle.mxfp8_dim0(np.ascontiguousarray(case.x[rows]), 0 if mode == "floor" else 1)
+    rows_d = torch.from_numpy(rows).cuda()
+    assert np.array_equal(s.index_select(0, rows_d).cpu().numpy(), rs)
+    assert np.array_equal(q.view(torch.uint8).index_select(0, rows_d).cpu().numpy(), rq)

@@ -157,3 +157,16 @@ def test_ex_calls_reject_unknown_flags(gq):
 ])
 def test_expert_dim1_host_validation(gq, args, status):
     assert gq.lib().gq_fp8_expert_dim1(*args, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    # x, M, K, out, scales, mode
+    ((A16, 4, 32, A16, A16, 2), 1),        # unknown mode
+    ((A16, 4, 48, A16, A16, 0), 2),        # K % 32
+    ((A16, -4, 32, A16, A16, 0), 1),       # negative M
+    ((A16, 4, 32, None, A16, 1), 1),       # NULL output
+    ((BAD, 4, 32, A16, A16, 1), 1),        # misaligned input
+    ((None, 0, 32, None, None, 0), 0),     # empty: nothing to do
+])
+def test_mxfp8_host_validation(gq, args, status):
+    assert gq.lib().gq_mxfp8_dim0(*args, None) == status

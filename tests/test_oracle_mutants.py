@@ -46,6 +46,10 @@ MUTANTS = {
     "rowwise_scale_layout": ("scales[n * n_groups + g] = s;",
                              "scales[g * N + n] = s;"),
     "pow2_rounds_up": ("return ldexpf(1.0f, e - 1);", "return ldexpf(1.0f, e);"),
+    "mx_floor_off_by_one": ("E = (e - 1) - 8;", "E = e - 8;"),
+    "mx_rceil_as_floor": ("E = (frexpf(v, &e) == 0.5f) ? e - 1 : e;",
+                          "frexpf(v, &e); E = e - 1;"),
+    "mx_zero_block": ("if (amax == 0.0f) return -127;", "if (amax == 0.0f) return 0;"),
     "expert_amax_ignores_expert": ("float a = fabsf(gqo_bf16_to_float(w[(e * K + k) * N + n]));",
                                    "float a = fabsf(gqo_bf16_to_float(w[k * N + n]));"),
     "pow2_ignored": ("return pow2 ? gqo_scale_pow2(amax) : gqo_scale(amax);",
