@@ -69,6 +69,7 @@ class Oracle:
         lib.gqo_expert_dim1.argtypes = [p, i64, i64, i64, ctypes.c_int, p, p]
         lib.gqo_expert_dim1.restype = ctypes.c_int
         lib.gqo_scale_pow2_array.argtypes = [p, i64, p]
+        lib.gqo_grouped_wgrad.argtypes = [p, p, p, p, i64, i64, i64, p, i32, p, p]
         lib.gqo_scale_pow2_array.restype = None
         lib.gqo_e4m3_encode_array.argtypes = [p, i64, p]
         lib.gqo_e4m3_decode_array.argtypes = [p, i64, p]
@@ -194,6 +195,30 @@ class Oracle:
         return q, s
 
 
+    def grouped_wgrad(self, qa_t, sa, qx, sx, offs):
+        """grad_weight per token group from the quantized operands: qa_t e4m3
+        codes (T, N), sa fp32 (N, G), qx e4m3 codes (T, K), sx fp32 (G, K).
+        Returns (out float64 (G, N, K), absum float64 (G, N, K)): the exact
+        sum of products divided by sa * sx, and the same for |products|."""
+        qa = _c(qa_t, np.uint8)
+        qxx = _c(qx, np.uint8)
+        o = _c(offs, np.int32)
+        T, N = qa.shape
+        T2, K = qxx.shape
+        assert T == T2
+        G = o.shape[0]
+        a_s = _c(sa, np.float32).reshape(N, G)
+        x_s = _c(sx, np.float32).reshape(G, K)
+        out = np.zeros((G, N, K), np.float64)
+        absum = np.zeros((G, N, K), np.float64)
+        rc = self.lib.gqo_grouped_wgrad(qa.ctypes.data, a_s.ctypes.data, qxx.ctypes.data,
+                                        x_s.ctypes.data, T, N, K, o.ctypes.data, G,
+                                        out.ctypes.data, absum.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle grouped_wgrad: invalid arguments")
+        return out, absum
+
+
 _lock = threading.Lock()
 _default: Oracle | None = None
 
@@ -241,6 +266,10 @@ def expert_dim1(w_bf16_bits, pow2=False):
 
 def mxfp8_dim0(x_bf16_bits, mode):
     return get().mxfp8_dim0(x_bf16_bits, mode)
+
+
+def grouped_wgrad(qa_t, sa, qx, sx, offs):
+    return get().grouped_wgrad(qa_t, sa, qx, sx, offs)
 
 
 def threads_used() -> int:

@@ -354,6 +354,83 @@ int gqo_mxfp8_dim0(const uint16_t* x, int64_t M, int64_t K, int mode, uint8_t* q
   return 0;
 }
 
+/* ------------------------------------------------ grouped grad_weight --- */
+
+/*
+ * The consumer of both quantized operands: the grad_weight GEMM of the MoE
+ * backward pass, one product per token group ("[moe training] use smaller
+ * block sizes for per group scaling kernels to improve perf" (#2668), MoE
+ * fp8 training test: grad_weight = grad_output_t @ input, token groups
+ * aligned to 16).  With
+ *   qa_t: e4m3 codes (T, N) row-major -- the rowwise_t output, grad_output_t
+ *         as a column-major (N, T) operand; sa: fp32 (N, G), its scales;
+ *   qx:   e4m3 codes (T, K) row-major -- the colwise output of the layer
+ *         input; sx: fp32 (G, K), its scales;
+ * the result for group g = [s_g, e_g) is
+ *   out[g][n][k] = ( sum over t in g of dec(qa_t[t][n]) * dec(qx[t][k]) )
+ *                  / ( sa[n][g] * sx[g][k] ),
+ * each quantized factor divided by the multiplier that produced it.
+ *
+ * Precision: double.  A product of two e4m3 values is exact (8 significant
+ * bits, a multiple of 2^-18, below 2^17.7), and so is every partial sum for
+ * T < 2^17 tokens (at most 53 bits); sa * sx is exact (two 24-bit
+ * significands); the quotient is the only rounding.  absum (may be NULL)
+ * receives the same quotient of the sum of |products|, the scale against
+ * which an fp32 accumulation error is measured.  An empty group gives zeros;
+ * tokens past the last end belong to no group.  Returns 0, or -1 on invalid
+ * arguments.
+ */
+int gqo_grouped_wgrad(const uint8_t* qa_t, const float* sa, const uint8_t* qx,
+                      const float* sx, int64_t T, int64_t N, int64_t K,
+                      const int32_t* offs, int32_t n_groups, double* out, double* absum) {
+  double dec[256];
+  int64_t *start, *end;
+  double *acc, *mag;
+  int64_t t, n, k;
+  int32_t g;
+  int c;
+  if (T < 0 || N < 0 || K < 0 || n_groups < 1 || offs == NULL) return -1;
+  if (N * K > 0 && (out == NULL || sa == NULL || sx == NULL)) return -1;
+  if (T * N > 0 && qa_t == NULL) return -1;
+  if (T * K > 0 && qx == NULL) return -1;
+  for (c = 0; c < 256; ++c) dec[c] = gqo_e4m3_decode((uint8_t)c);
+  start = (int64_t*)malloc(sizeof(int64_t) * (size_t)n_groups);
+  end = (int64_t*)malloc(sizeof(int64_t) * (size_t)n_groups);
+  acc = (double*)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
+  mag = (double*)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
+  if (!start || !end || !acc || !mag) {
+    free(start);
+    free(end);
+    free(acc);
+    free(mag);
+    return -1;
+  }
+  gqo_group_bounds(offs, n_groups, T, start, end);
+  for (g = 0; g < n_groups; ++g) {
+    for (n = 0; n < N * K; ++n) acc[n] = mag[n] = 0.0;
+    for (t = start[g]; t < end[g]; ++t)
+      for (n = 0; n < N; ++n) {
+        const double a = dec[qa_t[t * N + n]];
+        for (k = 0; k < K; ++k) {
+          const double p = a * dec[qx[t * K + k]];
+          acc[n * K + k] += p;
+          mag[n * K + k] += fabs(p);
+        }
+      }
+    for (n = 0; n < N; ++n)
+      for (k = 0; k < K; ++k) {
+        const double d = (double)sa[n * n_groups + g] * (double)sx[(int64_t)g * K + k];
+        out[((int64_t)g * N + n) * K + k] = acc[n * K + k] / d;
+        if (absum) absum[((int64_t)g * N + n) * K + k] = mag[n * K + k] / d;
+      }
+  }
+  free(start);
+  free(end);
+  free(acc);
+  free(mag);
+  return 0;
+}
+
 /* The plain method: scales exactly 448 / max(amax, 1e-12). */
 int gqo_colwise(const uint16_t* x, int64_t M, int64_t K, const int32_t* offs,
                 int32_t n_groups, uint8_t* q, float* scales) {

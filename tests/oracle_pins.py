@@ -418,6 +418,62 @@ def pin_mxfp8_dim0(o):
                 assert np.array_equal(q[r, 32 * b:32 * b + 32], want), (mode, r, b)
 
 
+
+def _torch_decode_f64(codes):
+    """torch's own e4m3 decode, in float64 (independent of the oracle's)."""
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_wgrad_hand(o):
+    """grad_weight per token group worked by hand: 4 tokens, groups [0, 1),
+    [1, 1) (empty) and [1, 3); token 3 belongs to no group.  Codes 0x38 = 1,
+    0x40 = 2, 0x30 = 0.5, 0xC8 = -4, 0xC0 = -2; the scales are powers of two,
+    so every quotient below is exact."""
+    qa = np.array([[0x38, 0x40], [0x30, 0xC8], [0x38, 0x38], [0x7E, 0x7E]], np.uint8)
+    qx = np.array([[0x40, 0x30], [0x38, 0x38], [0xC0, 0x38], [0x7E, 0xFE]], np.uint8)
+    sa = np.array([[2, 64, 4], [0.5, 64, 1]], np.float32)        # (N, G)
+    sx = np.array([[1, 8], [64, 64], [0.25, 2]], np.float32)      # (G, K)
+    out, absum = o.grouped_wgrad(qa, sa, qx, sx, np.array([1, 1, 3], np.int32))
+    # group 0: token 0 alone, a = (1, 2), x = (2, 0.5)
+    want0 = [[2 / (2 * 1), 0.5 / (2 * 8)], [4 / (0.5 * 1), 1 / (0.5 * 8)]]
+    # group 2: tokens 1 and 2: sums (-1.5, 1.5; -6, -3), |sums| (2.5, 1.5; 6, 5)
+    want2 = [[-1.5 / (4 * 0.25), 1.5 / (4 * 2)], [-6 / (1 * 0.25), -3 / (1 * 2)]]
+    abs2 = [[2.5 / (4 * 0.25), 1.5 / (4 * 2)], [6 / (1 * 0.25), 5 / (1 * 2)]]
+    assert np.array_equal(out[0], np.array(want0)), out[0]
+    assert np.array_equal(out[1], np.zeros((2, 2))), out[1]
+    assert np.array_equal(out[2], np.array(want2)), out[2]
+    assert np.array_equal(absum[2], np.array(abs2)), absum[2]
+
+
+def pin_wgrad_vs_matmul(o):
+    """Each group's result times sa * sx is the plain matrix product of the
+    decoded operands over the group's tokens (numpy's float64 matmul of
+    torch-decoded values: every product and sum is exact, so any summation
+    order gives the same numbers), with empty groups, ragged sizes and
+    uncovered tokens; the same for |products|."""
+    rng = np.random.default_rng(59)
+    T, N, K = 150, 40, 24
+    offs = np.array([13, 13, 61, 100, 141], np.int32)   # an empty group; 9 tokens uncovered
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    qa = rng.choice(finite, size=(T, N))
+    qx = rng.choice(finite, size=(T, K))
+    G = offs.shape[0]
+    sa = (np.exp2(rng.integers(-10, 11, (N, G))) * rng.uniform(1, 2, (N, G))).astype(np.float32)
+    sx = (np.exp2(rng.integers(-10, 11, (G, K))) * rng.uniform(1, 2, (G, K))).astype(np.float32)
+    out, absum = o.grouped_wgrad(qa, sa, qx, sx, offs)
+    da, dx = _torch_decode_f64(qa), _torch_decode_f64(qx)
+    s0 = 0
+    for g in range(G):
+        e = int(offs[g])
+        d = sa[:, g].astype(np.float64)[:, None] * sx[g].astype(np.float64)[None, :]
+        want = da[s0:e].T @ dx[s0:e]
+        wabs = np.abs(da[s0:e]).T @ np.abs(dx[s0:e])
+        assert np.allclose(out[g] * d, want, rtol=2.0 ** -50, atol=0), g
+        assert np.allclose(absum[g] * d, wabs, rtol=2.0 ** -50, atol=0), g
+        s0 = e
+
+
 ALL_PINS = [
     pin_decode_landmarks, pin_decode_vs_torch, pin_encode_roundtrip,
     pin_encode_midpoints, pin_encode_boundaries, pin_encode_vs_torch,
@@ -425,4 +481,5 @@ ALL_PINS = [
     pin_paths_vs_library_loop, pin_out_of_contract_offsets,
     pin_transpose_identity, pin_max_code_invariant, pin_dequant_bound,
     pin_scale_pow2, pin_pow2_paths, pin_expert_dim1, pin_mxfp8_dim0,
+    pin_wgrad_hand, pin_wgrad_vs_matmul,
 ]

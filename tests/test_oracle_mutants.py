@@ -52,6 +52,14 @@ MUTANTS = {
     "mx_zero_block": ("if (amax == 0.0f) return -127;", "if (amax == 0.0f) return 0;"),
     "expert_amax_ignores_expert": ("float a = fabsf(gqo_bf16_to_float(w[(e * K + k) * N + n]));",
                                    "float a = fabsf(gqo_bf16_to_float(w[k * N + n]));"),
+    "wgrad_drops_last_token": ("for (t = start[g]; t < end[g]; ++t)\n      for (n = 0; n < N; ++n) {",
+                               "for (t = start[g]; t + 1 < end[g]; ++t)\n      for (n = 0; n < N; ++n) {"),
+    "wgrad_operand_transposed": ("const double a = dec[qa_t[t * N + n]];",
+                                 "const double a = dec[qa_t[n * T + t]];"),
+    "wgrad_scale_of_wrong_group": ("(double)sa[n * n_groups + g]",
+                                   "(double)sa[n * n_groups + (g > 0 ? g - 1 : 0)]"),
+    "wgrad_sx_ignored": (" * (double)sx[(int64_t)g * K + k];", ";"),
+    "wgrad_abs_dropped": ("mag[n * K + k] += fabs(p);", "mag[n * K + k] += p;"),
     "pow2_ignored": ("return pow2 ? gqo_scale_pow2(amax) : gqo_scale(amax);",
                      "return gqo_scale(amax);"),
 }
