@@ -384,6 +384,97 @@ def run_mxfp8(args):
     return 0
 
 
+WGRAD_SHAPE = (16640, 8192, 4096, 16)  # tokens T, N, K, groups
+
+
+def run_wgrad(args):
+    """Times the grouped grad_weight GEMM on the tensor cores: T = 16640 tokens
+    in 16 groups (the rowwise_t workload's tokens), N = 8192, K = 4096, e4m3
+    operands with fp32 scales, bf16 out.  One call = one step."""
+    import numpy as np
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import fp8_quantization_moe_gb300 as gq
+    from fp8_quantization_moe_gb300 import synth
+
+    T, N, K, G = WGRAD_SHAPE
+    rng = np.random.default_rng(1700)
+    offs_np = synth.random_partition(rng, T, G)
+    c = synth.wgrad_case(T, N, K, offs_np, seed=1701)
+    qa = torch.from_numpy(c.qa_t).to(dev)
+    qx = torch.from_numpy(c.qx).to(dev)
+    sa = torch.from_numpy(c.sa).to(dev)
+    sx = torch.from_numpy(c.sx).to(dev)
+    offs = torch.from_numpy(c.offs).to(dev)
+    out = torch.empty((G, N, K), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        gq.grouped_wgrad(qa, sa, qx, sx, offs, out=out, stream=stream)
+    torch.cuda.synchronize(dev)
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(f"GPU-{props.uuid}")
+    sampler.start()
+    time.sleep(0.3)
+    sampler.t_load[0] = time.time()
+    t_end = time.time() + args.clock_window
+    while time.time() < t_end:
+        for _ in range(5):
+            gq.grouped_wgrad(qa, sa, qx, sx, offs, out=out, stream=stream)
+        torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        gq.grouped_wgrad(qa, sa, qx, sx, offs, out=out, stream=stream)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.t_load[1] = time.time()
+    sampler.stop()
+    gq.check_device_error()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    flops = 2.0 * N * K * int(offs_np[-1])
+    tflops = flops * args.steps / (total_ms * 1e-3) / 1e12
+    peak, peak_kind = measured_tensor_peak_fp8()
+    out_bytes = G * N * K * 2
+    line = {
+        "metric": "grouped fp8 grad_weight GEMM throughput (tensor cores)", "value": tflops,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> fp32 accumulate -> bf16", "data": "synthetic (seeded e4m3 codes)",
+        "config": {"workload": f"grad_weight per token group: T={T} tokens in {G} groups, "
+                               f"N={N}, K={K}; out bf16 ({G}, {N}, {K})",
+                   "l2": f"output {out_bytes / 2**30:.2f} GiB larger than L2 per call; no flush"},
+        "per_call": {"us_median": statistics.median(per) * 1e3,
+                     "timing": "CUDA events on the launching stream around each call"},
+        "roofline": {"bound": "tensor", "kernel": "wgrad_kernel", "achieved": tflops,
+                     "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_kind": peak_kind, "traffic": None, "algorithmic_flops": flops,
+                     "hbm_floor_us": (out_bytes + T * (N + K)) / (measured_peaks()[0] * 1e3)},
+        "clocks": sampler.summary(),
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def measured_tensor_peak_fp8():
+    """fp8 dense peak: the measured cuBLAS bf16 burst figure times the nominal
+    fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s), else the fallback bf16 figure times
+    the same ratio."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "measured bf16 x 2 (nominal fp8/bf16)"
+    except (OSError, KeyError, ValueError):
+        return 2.0 * 1900.0, "fallback bf16 x 2 (nominal fp8/bf16)"
+
+
 def run_mine(args):
     import numpy as np
     import torch
@@ -594,6 +685,8 @@ def main(argv=None):
     ap.add_argument("--mxfp8", choices=["floor", "rceil"], default=None,
                     help="time the mxfp8 dim0 cast of the colwise input instead "
                          "of the main step")
+    ap.add_argument("--wgrad", action="store_true",
+                    help="time the grouped fp8 grad_weight GEMM instead of the main step")
     ap.add_argument("--half", action="store_true",
                     help="profiling case: half the tokens of each workload "
                          "(inputs 256 MB and 136 MB, still larger than L2); "
@@ -613,6 +706,8 @@ def main(argv=None):
         return run_expert(args)
     if args.mxfp8:
         return run_mxfp8(args)
+    if args.wgrad:
+        return run_wgrad(args)
     return run_mine(args)
 
 

@@ -9,7 +9,9 @@ Two paths, both in hand-written sm_103a CUDA kernels behind the C ABI of
 * ``expert_dim1(w)``     -- stacked expert weights (E, K, N): one scale per
   (expert, column), reduced along dim1;
 * ``mxfp8_dim0(x, mode)`` -- mxfp8: 32-element row blocks with e8m0 scales
-  (FLOOR or RCEIL).
+  (FLOOR or RCEIL);
+* ``grouped_wgrad(qa_t, sa, qx, sx, offs)`` -- the consumer of the two
+  paths: grad_weight per token group on the tensor cores, bf16 out.
 
 scale = 448 / max(amax, 1e-12) in IEEE fp32; q = saturating round-to-nearest-
 even e4m3 cast of fp32(x * scale); ``pow2_scales=True`` rounds every scale
@@ -20,7 +22,7 @@ supplies device memory and streams.  ``synth`` draws seeded inputs.
 from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
                        GQ_SCALE_POW2, GQError, check_device_error, colwise, colwise_host,
                        colwise_noalloc, expert_dim1, mxfp8_dim0,
-                       debug_set, lib, library_path, rowwise_t,
+                       grouped_wgrad, debug_set, lib, library_path, rowwise_t,
                        rowwise_t_host, set_lag, status_string, version,
                        workspace_bytes)
 from ._build import build
@@ -28,7 +30,7 @@ from ._build import build
 __all__ = [
     "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQ_SCALE_POW2", "GQError",
     "build", "check_device_error", "colwise", "colwise_host",
-    "colwise_noalloc", "debug_set", "expert_dim1", "mxfp8_dim0",
+    "colwise_noalloc", "debug_set", "expert_dim1", "grouped_wgrad", "mxfp8_dim0",
     "lib", "library_path", "rowwise_t", "rowwise_t_host", "set_lag",
     "status_string",
     "version", "workspace_bytes",

@@ -37,6 +37,7 @@ SIGNATURES = {
     "gq_fp8_colwise_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
     "gq_fp8_expert_dim1": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
     "gq_mxfp8_dim0": (ctypes.c_int, [_P, _I64, _I64, _P, _P, ctypes.c_int, _P]),
+    "gq_grouped_wgrad": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I32, _P, _P]),
     "gq_fp8_rowwise_t_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
     "gq_check_device_error": (ctypes.c_int, [_P]),
     "gq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -279,6 +280,41 @@ def mxfp8_dim0(x: torch.Tensor, mode: str = "floor", *, out=None, scales=None, s
         st = lib().gq_mxfp8_dim0(_ptr(x), M, K, _ptr(out), _ptr(scales), modes[mode], sh)
     _check(st, "gq_mxfp8_dim0")
     return out, scales
+
+
+def grouped_wgrad(qa_t: torch.Tensor, sa: torch.Tensor, qx: torch.Tensor, sx: torch.Tensor,
+                  offs: torch.Tensor, *, out=None, stream=None):
+    """grad_weight per token group from the quantized operands: qa_t e4m3
+    (T, N) (the rowwise_t output), sa float32 (N, G), qx e4m3 (T, K) (the
+    colwise output), sx float32 (G, K), offs int32 (G,) end offsets along T.
+    Returns out bf16 (G, N, K) = the per-group sum of products divided by
+    sa * sx."""
+    for name, t, nd in (("qa_t", qa_t, 2), ("qx", qx, 2)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.element_size() == 1
+                and t.dim() == nd and t.is_contiguous()):
+            raise ValueError(f"grouped_wgrad: {name} must be a contiguous 2-D 1-byte CUDA tensor")
+    T, N = qa_t.shape
+    T2, K = qx.shape
+    if T2 != T:
+        raise ValueError("grouped_wgrad: qa_t and qx must have the same number of tokens")
+    if not (offs.is_cuda and offs.dtype == torch.int32 and offs.dim() == 1 and offs.is_contiguous()):
+        raise ValueError("grouped_wgrad: offs must be a contiguous 1-D int32 CUDA tensor")
+    G = offs.shape[0]
+    for name, t, shape in (("sa", sa, (N, G)), ("sx", sx, (G, K))):
+        if not (t.is_cuda and t.dtype == torch.float32 and tuple(t.shape) == shape
+                and t.is_contiguous()):
+            raise ValueError(f"grouped_wgrad: {name} must be a contiguous float32 {shape} CUDA tensor")
+    dev = qa_t.device
+    if out is None:
+        out = torch.empty((G, N, K), dtype=torch.bfloat16, device=dev)
+    if out.shape != (G, N, K) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("grouped_wgrad: out must be a contiguous bf16 (G, N, K) tensor")
+    sh = _stream_handle(stream, dev)
+    with torch.cuda.device(dev):
+        st = lib().gq_grouped_wgrad(_ptr(qa_t), _ptr(sa), _ptr(qx), _ptr(sx), T, N, K,
+                                    _ptr(offs), G, _ptr(out), sh)
+    _check(st, "gq_grouped_wgrad")
+    return out
 
 
 def colwise_noalloc(x: torch.Tensor, offs: torch.Tensor, *, out=None,

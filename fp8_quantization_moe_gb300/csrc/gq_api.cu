@@ -76,6 +76,8 @@ void setup_device(int dev) {
   st = rowwise::setup(info);
   if (st != GQ_OK) return;
   st = mx::setup(info);
+  if (st != GQ_OK) return;
+  st = wgrad::setup(info);
 }
 
 // Set-up for the current device (once per device per process).
@@ -388,6 +390,40 @@ gq_status gq_mxfp8_dim0(const void* x, int64_t M, int64_t K, void* out, uint8_t*
   gq_status st = current_device(&info);
   if (st != GQ_OK) return st;
   return mx::launch(*info, x, M, K, out, scales, mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gq_status gq_grouped_wgrad(const void* qa_t, const float* sa, const void* qx, const float* sx,
+                           int64_t T, int64_t N, int64_t K, const int32_t* offs,
+                           int32_t n_groups, void* out, gq_stream_t stream) {
+  const char* name = "gq_grouped_wgrad";
+  if (T < 0 || N < 0 || K < 0)
+    return fail(GQ_ERR_INVALID_ARG, "%s: negative size (%lld, %lld, %lld)", name,
+                static_cast<long long>(T), static_cast<long long>(N), static_cast<long long>(K));
+  if (n_groups < 1 || n_groups > GQ_MAX_GROUPS)
+    return fail(GQ_ERR_INVALID_ARG, "%s: n_groups = %d out of range", name, n_groups);
+  if (T > kMaxExtent || N > kMaxExtent || K > kMaxExtent)
+    return fail(GQ_ERR_UNSUPPORTED, "%s: extent >= 2^31", name);
+  if (N % 16 != 0 || K % 16 != 0)
+    return fail(GQ_ERR_UNSUPPORTED, "%s: N = %lld and K = %lld must be multiples of 16", name,
+                static_cast<long long>(N), static_cast<long long>(K));
+  if (N == 0 || K == 0) return GQ_OK;
+  if (out == nullptr || sa == nullptr || sx == nullptr || offs == nullptr)
+    return fail(GQ_ERR_INVALID_ARG, "%s: NULL pointer", name);
+  if (!aligned(out, 16) || !aligned(sa, 4) || !aligned(sx, 4))
+    return fail(GQ_ERR_INVALID_ARG, "%s: misaligned output or scales", name);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t out_bytes = static_cast<size_t>(n_groups) * N * K * 2;
+  if (T == 0)  // every group is empty
+    return check_cuda(cudaMemsetAsync(out, 0, out_bytes, s), "grouped_wgrad: zero output");
+  if (qa_t == nullptr || qx == nullptr)
+    return fail(GQ_ERR_INVALID_ARG, "%s: NULL operand", name);
+  if (!aligned(qa_t, 16) || !aligned(qx, 16))
+    return fail(GQ_ERR_INVALID_ARG, "%s: operands must be 16-byte aligned", name);
+  const DeviceInfo* info = nullptr;
+  gq_status st = current_device(&info);
+  if (st != GQ_OK) return st;
+  return wgrad::launch(*info, g_dbg, qa_t, sa, qx, sx, static_cast<int32_t>(T),
+                       static_cast<int32_t>(N), static_cast<int32_t>(K), offs, n_groups, out, s);
 }
 
 gq_status gq_check_device_error(gq_stream_t stream) {

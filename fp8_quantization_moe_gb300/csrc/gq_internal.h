@@ -81,6 +81,13 @@ gq_status launch(const DeviceInfo& info, const void* x, int64_t M, int64_t K, vo
                  uint8_t* scales, int mode, cudaStream_t stream);
 }  // namespace mx
 
+namespace wgrad {
+gq_status setup(DeviceInfo& info);
+gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* qa_t, const float* sa,
+                 const void* qx, const float* sx, int32_t T, int32_t N, int32_t K,
+                 const int32_t* offs, int32_t G, void* out, cudaStream_t stream);
+}  // namespace wgrad
+
 // Writes the scale of an empty group -- 448 / 1e-12 (fp32), or its power
 // of two below with GQ_SCALE_POW2 -- into n scales: every group is empty
 // when the token extent is 0.

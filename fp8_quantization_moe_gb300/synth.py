@@ -216,3 +216,34 @@ def random_case(kind: str, rows: int, cols: int, n_groups: int, seed: int,
         offs = np.asarray(ends, dtype=np.int32)
     return Case(f"{kind}_{rows}x{cols}_g{n_groups}_s{seed}", kind,
                 to_bf16_bits(x), offs, seed)
+
+
+@dataclass
+class WgradCase:
+    """Operands of the grouped grad_weight product: e4m3 codes qa_t (T, N)
+    and qx (T, K) as uint8, their fp32 scales sa (N, G) and sx (G, K), and
+    int32 end offsets along T."""
+    name: str
+    qa_t: np.ndarray
+    sa: np.ndarray
+    qx: np.ndarray
+    sx: np.ndarray
+    offs: np.ndarray
+
+
+# every e4m3 code but the two NaN codes (S.1111.111)
+_FINITE_E4M3 = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+
+
+def wgrad_case(T: int, N: int, K: int, offs, seed: int) -> WgradCase:
+    """Codes drawn uniformly from the finite e4m3 codes (magnitudes 2^-9 to
+    448, both signs, zeros), scales 2^U{-12..12} * U(1, 2) -- the ranges the
+    two quantizers produce, without their arithmetic."""
+    rng = np.random.default_rng(seed)
+    offs = np.asarray(offs, np.int32)
+    G = offs.shape[0]
+    qa_t = rng.choice(_FINITE_E4M3, size=(T, N))
+    qx = rng.choice(_FINITE_E4M3, size=(T, K))
+    sa = (np.exp2(rng.integers(-12, 13, (N, G))) * rng.uniform(1, 2, (N, G))).astype(np.float32)
+    sx = (np.exp2(rng.integers(-12, 13, (G, K))) * rng.uniform(1, 2, (G, K))).astype(np.float32)
+    return WgradCase(f"wgrad_{T}x{N}x{K}_g{G}", qa_t, sa, qx, sx, offs)

@@ -204,6 +204,40 @@ gq_status gq_mxfp8_dim0(const void* x, int64_t M, int64_t K, void* out, uint8_t*
                         int mode, gq_stream_t stream);
 
 /*
+ * The grad_weight GEMM of the MoE backward pass, one product per token group,
+ * from the two quantized operands (pytorch/ao page "[moe training] use
+ * smaller block sizes for per group scaling kernels to improve perf", MoE
+ * fp8 training test: grad_weight = grad_output_t @ input, token groups):
+ *
+ *   out[g][n][k] = bf16( acc * (1 / sa[n][g]) * (1 / sx[g][k]) ),
+ *   acc = sum over tokens t of group g of e4m3(qa_t[t][n]) * e4m3(qx[t][k]),
+ *
+ * acc accumulated in fp32 on the tensor cores (order unspecified),
+ * reciprocals and products in IEEE fp32, bf16 by round-to-nearest-even.
+ *
+ *   qa_t     e4m3 [T, N] row-major (the gq_fp8_rowwise_t output: grad_output_t
+ *            as a column-major (N, T) operand), 16-byte aligned.  (input)
+ *   sa       fp32 [N, n_groups], the scales that produced qa_t.  (input)
+ *   qx       e4m3 [T, K] row-major (the gq_fp8_colwise output of the layer
+ *            input), 16-byte aligned.                            (input)
+ *   sx       fp32 [n_groups, K], the scales that produced qx.    (input)
+ *   T, N, K  >= 0, N % 16 == 0 and K % 16 == 0, each below 2^31.
+ *   offs     device int32 [n_groups], END offsets along T (as for the other
+ *            calls: running maximum, clamped to [0, T]); tokens past the last
+ *            end belong to no group.                             (input)
+ *   n_groups 1 .. GQ_MAX_GROUPS.
+ *   out      bf16 [n_groups, N, K] row-major, 16-byte aligned; a group with
+ *            no tokens gets zeros.                               (output)
+ *   stream   the CUDA stream to run on.  No workspace.
+ * Returns GQ_ERR_INVALID_ARG for a NULL or misaligned pointer, a negative
+ * size or n_groups out of range; GQ_ERR_UNSUPPORTED for N or K not a
+ * multiple of 16 or an extent of 2^31 or more.
+ */
+gq_status gq_grouped_wgrad(const void* qa_t, const float* sa, const void* qx, const float* sx,
+                           int64_t T, int64_t N, int64_t K, const int32_t* offs,
+                           int32_t n_groups, void* out, gq_stream_t stream);
+
+/*
  * Colwise scaling with no allocation at all, not even a caller workspace.
  * The pytorch/ao pages have no counterpart to this entry point; it exists for
  * callers that cannot obtain device memory at the point where they quantize

@@ -170,3 +170,21 @@ def test_expert_dim1_host_validation(gq, args, status):
 ])
 def test_mxfp8_host_validation(gq, args, status):
     assert gq.lib().gq_mxfp8_dim0(*args, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    # qa_t, sa, qx, sx, T, N, K, offs, G, out
+    ((A16, A16, A16, A16, -1, 16, 16, A16, 1, A16), 1),    # negative T
+    ((A16, A16, A16, A16, 16, 16, 16, A16, 0, A16), 1),    # no groups
+    ((A16, A16, A16, A16, 16, 16, 16, A16, 1025, A16), 1),  # > GQ_MAX_GROUPS
+    ((A16, A16, A16, A16, 16, 24, 16, A16, 1, A16), 2),    # N % 16
+    ((A16, A16, A16, A16, 16, 16, 40, A16, 1, A16), 2),    # K % 16
+    ((A16, A16, A16, A16, 16, 16, 16, A16, 1, None), 1),   # NULL output
+    ((A16, A16, A16, A16, 16, 16, 16, None, 1, A16), 1),   # NULL offsets
+    ((None, A16, A16, A16, 16, 16, 16, A16, 1, A16), 1),   # NULL operand
+    ((BAD, A16, A16, A16, 16, 16, 16, A16, 1, A16), 1),    # misaligned operand
+    ((A16, A16, A16, A16, 16, 16, 16, A16, 1, BAD), 1),    # misaligned output
+    ((None, None, None, None, 16, 0, 16, None, 1, None), 0),  # N == 0: nothing to do
+])
+def test_grouped_wgrad_host_validation(gq, args, status):
+    assert gq.lib().gq_grouped_wgrad(*args, None) == status
