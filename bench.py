@@ -402,7 +402,8 @@ def run_wgrad(args):
     import fp8_quantization_moe_gb300 as gq
     from fp8_quantization_moe_gb300 import synth
 
-    T, N, K, G = WGRAD_SHAPE
+    T, N, K, G = (tuple(int(v) for v in args.wgrad_shape.split(",")) if args.wgrad_shape
+                  else WGRAD_SHAPE)
     rng = np.random.default_rng(1700)
     offs_np = synth.random_partition(rng, T, G)
     c = synth.wgrad_case(T, N, K, offs_np, seed=1701)
@@ -687,6 +688,8 @@ def main(argv=None):
                          "of the main step")
     ap.add_argument("--wgrad", action="store_true",
                     help="time the grouped fp8 grad_weight GEMM instead of the main step")
+    ap.add_argument("--wgrad-shape", default=None,
+                    help="T,N,K,groups for --wgrad (a smaller case for profiling)")
     ap.add_argument("--half", action="store_true",
                     help="profiling case: half the tokens of each workload "
                          "(inputs 256 MB and 136 MB, still larger than L2); "

@@ -19,12 +19,13 @@
 //   warp 1: allocates the 512 TMEM columns (two accumulators of 256 fp32
 //     columns, so that a tile's epilogue overlaps the next tile's MMAs);
 //     zeroes the token rows of a group's last chunk that lie past its end;
-//     one lane issues tcgen05.mma kind::f8f6f4 (M = 128, N = 128, K = 32,
+//     one lane issues tcgen05.mma kind::f8f6f4 (M = 128, N = 256, K = 32,
 //     both operands MN-major: the token index is the contraction index and
 //     the operands are contiguous along n and k) and commits each stage back
 //     to the producer and each finished accumulator to the epilogue;
-//   warps 2-5: each reads its 32 TMEM lanes (rows n) with tcgen05.ld, scales,
-//     rounds to bf16 and stores its rows' 512-byte runs of the tile.
+//   warps 2-5: each reads its 32 TMEM lanes (rows n) with tcgen05.ld, 64
+//     columns at a time, scales, rounds to bf16, stages the 32 rows' 128-byte
+//     runs in shared memory and stores them as whole lines.
 // A group with no tokens gets zeros from the epilogue without any MMA.
 // Every wait is bounded; on expiry the error word is set, the warp leaves
 // its loop (as a whole: the lanes agree through __all_sync), the others time out in turn, loads and MMAs still in flight are
@@ -37,19 +38,24 @@
 namespace gq {
 namespace wgrad {
 
-constexpr int kBM = 128;    // rows n of a tile (the MMA's M)
-constexpr int kHalfN = 128;  // columns k per MMA (the MMA's N)
-constexpr int kBN = 2 * kHalfN;  // columns k of a tile
+constexpr int kBM = 128;     // rows n of a tile (the MMA's M)
+constexpr int kHalfN = 128;  // columns k per swizzle atom (128 e4m3 bytes), one TMA box
+constexpr int kBN = 2 * kHalfN;  // columns k of a tile (the MMA's N)
 constexpr int kBK = 128;    // tokens per stage
 constexpr int kSubK = 32;   // tokens per MMA (kind::f8f6f4)
 constexpr int kStages = 4;
 constexpr int kABytes = kBK * kBM;         // 16 KB
 constexpr int kBHalfBytes = kBK * kHalfN;  // 16 KB
 constexpr int kStageBytes = kABytes + 2 * kBHalfBytes;
+// Stage layout: the two qx boxes (k 0-127, k 128-255), then the qa_t box.
+constexpr int kBOff = 0;
+constexpr int kAOff = 2 * kBHalfBytes;
 constexpr int kAccCols = kBN;              // fp32 TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kChunk = 64;                  // accumulator columns per epilogue step
+constexpr int kRowPitch = kChunk * 2 + 16;  // staged bf16 row: 128 bytes + 16 of padding
 static_assert(kTmemCols == 512, "two accumulators fill the TMEM");
 static_assert(kBM == 128 && kHalfN == 128 && kBK % kSubK == 0, "MMA shape");
 
@@ -62,6 +68,9 @@ struct Smem {
   uint64_t drain;             // the MMA warp's last commit
   uint32_t tmem_base;
   int32_t ends[kMaxGroups];
+  // per epilogue warp: 1/sx of the tile's columns, and 32 staged output rows
+  float rx[kEpiWarps][kBN];
+  alignas(16) uint8_t rows[kEpiWarps][32 * kRowPitch];
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
@@ -121,32 +130,51 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
                : "r"(taddr)
                : "memory");
 }
+// Keeps the registers of a TMEM load from being used before the wait that
+// precedes this point.
+__device__ __forceinline__ void tmem_pin(uint32_t (&r)[32]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) : : "memory");
+}
 // Waits for this thread's TMEM loads; the registers pass through the asm so
 // that no use of them is scheduled before it.
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) : : "memory");
 }
 
+// 16-byte shared load ordered after the warp's preceding shared stores
+// (volatile, with a memory clobber).
+__device__ __forceinline__ uint4 lds128_ordered(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Shared-memory matrix descriptor of one operand sub-tile: MN-major, 128-byte
-// swizzle, exactly one swizzle atom (128 bytes = 128 e4m3 values) along
-// M or N, groups of 8 token rows 1024 bytes apart.  Fields: start address
-// >> 4 (bits 0-13), leading byte offset >> 4 (16-29; the stride between
-// atoms along M/N, never used with one atom), stride byte offset >> 4
-// (32-45), descriptor version 1 (46-47), base offset 0 (49-51: atoms are
-// 1024-byte aligned), swizzle mode 2 = 128 bytes (61-63).
-__device__ __forceinline__ uint64_t operand_desc(uint32_t saddr) {
+// swizzle; a swizzle atom is 8 token rows x 128 bytes (128 e4m3 values along
+// M or N), atoms along the token index 1024 bytes apart, atoms along M or N
+// `lbo` bytes apart.  Fields: start address >> 4 (bits 0-13), leading byte
+// offset >> 4 (16-29: for swizzled MN-major operands the stride between
+// atoms along M or N), stride byte offset >> 4 (32-45: the stride between
+// 8-row groups along the token index), descriptor version 1 (46-47), base
+// offset 0 (49-51: atoms are 1024-byte aligned), swizzle mode 2 = 128 bytes
+// (61-63).
+__device__ __forceinline__ uint64_t operand_desc(uint32_t saddr, uint32_t lbo) {
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-         (static_cast<uint64_t>(1024u >> 4) << 16) |
+         (static_cast<uint64_t>(lbo >> 4) << 16) |
          (static_cast<uint64_t>(1024u >> 4) << 32) | (uint64_t(1) << 46) |
          (uint64_t(2) << 61);
 }
 
 // Instruction descriptor, kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B e4m3
 // (bits 7-9, 10-12 = 0), A and B MN-major (bits 15, 16), N >> 3 (17-22),
-// M >> 4 (24-28).
+// M >> 4 (24-28).  M = 128, N = 256: one MMA covers the whole tile.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | (1u << 16) |
-                            (static_cast<uint32_t>(kHalfN >> 3) << 17) |
+                            (static_cast<uint32_t>(kBN >> 3) << 17) |
                             (static_cast<uint32_t>(kBM >> 4) << 24);
+static_assert((kBN >> 3) < 64 && (kBM >> 4) < 32, "descriptor field widths");
 
 struct TileId {
   int32_t g, n0, k0, t0, tg;  // group, first row, first column, first token, tokens
@@ -213,10 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           uint8_t* base = s.stage[st];
           mbar_arrive_expect_tx(&s.full[st], kStageBytes);
-          tma_load_2d(base, &amap, t.n0, t.t0 + c, &s.full[st], pol);
-          tma_load_2d(base + kABytes, &xmap, t.k0, t.t0 + c, &s.full[st], pol);
-          tma_load_2d(base + kABytes + kBHalfBytes, &xmap, t.k0 + kHalfN, t.t0 + c, &s.full[st],
+          tma_load_2d(base + kBOff, &xmap, t.k0, t.t0 + c, &s.full[st], pol);
+          tma_load_2d(base + kBOff + kBHalfBytes, &xmap, t.k0 + kHalfN, t.t0 + c, &s.full[st],
                       pol);
+          tma_load_2d(base + kAOff, &amap, t.n0, t.t0 + c, &s.full[st], pol);
         }
       }
       // the block must not exit while a load is still writing its memory
@@ -258,14 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t a0 = smem_addr(base);
-          const uint32_t b0 = a0 + kABytes;
-          const uint32_t b1 = b0 + kBHalfBytes;
+          const uint32_t a0 = smem_addr(base + kAOff);
+          const uint32_t b0 = smem_addr(base + kBOff);
           for (int32_t j = 0; j < used; j += kSubK) {
             const uint32_t off = static_cast<uint32_t>(j * 128);  // 32 rows = 4 atoms
             const uint32_t acc = (c > 0 || j > 0) ? 1u : 0u;
-            tc_mma_e4m3(d, operand_desc(a0 + off), operand_desc(b0 + off), kIdesc, acc);
-            tc_mma_e4m3(d + kHalfN, operand_desc(a0 + off), operand_desc(b1 + off), kIdesc, acc);
+            // A: one atom along n; B: two atoms along k, one box apart
+            tc_mma_e4m3(d, operand_desc(a0 + off, 1024u), operand_desc(b0 + off, kBHalfBytes),
+                        kIdesc, acc);
           }
           tc_commit(&s.empty[st]);
           issued = true;
@@ -284,53 +312,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- epilogue --
+    // Lane l of epilogue warp q owns row n0 + 32 q + l of the tile.  Per
+    // step of 64 columns it reads its row's accumulators, scales them,
+    // packs bf16 and writes the 128-byte run into the warp's staging rows;
+    // the warp then stores the 32 runs as whole lines, four rows per
+    // instruction.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int ew = warp - 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    float* rx = s.rx[ew];
+    uint8_t* rows = s.rows[ew];
+    const uint32_t my_row = smem_addr(rows + lane * kRowPitch);
     uint32_t tc = 0;
     bool ok = true;
     for (int64_t i = blockIdx.x; ok && i < p.tiles; i += gridDim.x) {
       const TileId t = tile_of(p, s.ends, i);
-      const int32_t n = t.n0 + 32 * q + lane;
-      const bool row_ok = n < p.N;
-      uint16_t* orow = p.out + (static_cast<int64_t>(t.g) * p.N + n) * p.K;
-      if (t.tg <= 0) {
-        if (row_ok)
-          for (int32_t k = t.k0; k < t.k0 + kBN && k < p.K; k += 8)
-            __stcs(reinterpret_cast<uint4*>(orow + k), make_uint4(0u, 0u, 0u, 0u));
-        continue;
-      }
-      const int b = static_cast<int>(tc & 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(&s.acc_full[b], (tc >> 1) & 1, wait_ns, p.err));
-      if (!ok) break;
-      tc_fence_after();
-      const float ra = row_ok ? __frcp_rn(__ldg(p.sa + static_cast<int64_t>(n) * p.G + t.g)) : 0.0f;
+      const int32_t nbase = t.n0 + 32 * q;
+      const bool empty_group = t.tg <= 0;
+      // 1/sx of the tile's columns (0 past K)
       const float* sxg = p.sx + static_cast<int64_t>(t.g) * p.K;
-#pragma unroll 1
-      for (int ch = 0; ch < kBN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(b * kAccCols + ch * 32), r);
-        tmem_ld_wait(r);
-        const int32_t kc = t.k0 + ch * 32;
-        if (!row_ok || kc >= p.K) continue;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int32_t k = kc + 8 * v;
-          if (k >= p.K) break;
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = __uint_as_float(r[8 * v + 2 * e]) * ra * __frcp_rn(__ldg(sxg + k + 2 * e));
-            const float x1 = __uint_as_float(r[8 * v + 2 * e + 1]) * ra * __frcp_rn(__ldg(sxg + k + 2 * e + 1));
-            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-            w[e] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-          __stcs(reinterpret_cast<uint4*>(orow + k), make_uint4(w[0], w[1], w[2], w[3]));
-        }
+      __syncwarp();  // the previous tile's readers of rx are done
+      if (!empty_group)
+        for (int j = lane; j < kBN; j += 32)
+          rx[j] = t.k0 + j < p.K ? __frcp_rn(__ldg(sxg + t.k0 + j)) : 0.0f;
+      const int32_t n = nbase + lane;
+      const float ra =
+          (!empty_group && n < p.N) ? __frcp_rn(__ldg(p.sa + static_cast<int64_t>(n) * p.G + t.g))
+                                    : 0.0f;
+      const int b = static_cast<int>(tc & 1);
+      if (!empty_group) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&s.acc_full[b], (tc >> 1) & 1, wait_ns, p.err));
+        if (!ok) break;
+        tc_fence_after();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.acc_empty[b]);
-      ++tc;
+      __syncwarp();  // rx visible to the warp
+#pragma unroll 1
+      for (int ch = 0; ch < kBN / kChunk; ++ch) {
+        const int32_t kc = t.k0 + ch * kChunk;
+        uint32_t w[32];
+        if (!empty_group) {
+          uint32_t r0[32], r1[32];
+          const uint32_t ta = tmem + lane_base + static_cast<uint32_t>(b * kAccCols + ch * kChunk);
+          tmem_ld32(ta, r0);
+          tmem_ld32(ta + 32, r1);
+          tmem_ld_wait(r0);
+          tmem_pin(r1);
+          const float* rxc = rx + ch * kChunk;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat162 h0 = __floats2bfloat162_rn(
+                __uint_as_float(r0[2 * e]) * ra * rxc[2 * e],
+                __uint_as_float(r0[2 * e + 1]) * ra * rxc[2 * e + 1]);
+            const __nv_bfloat162 h1 = __floats2bfloat162_rn(
+                __uint_as_float(r1[2 * e]) * ra * rxc[32 + 2 * e],
+                __uint_as_float(r1[2 * e + 1]) * ra * rxc[32 + 2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&h0);
+            w[16 + e] = *reinterpret_cast<const uint32_t*>(&h1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = 0u;
+        }
+        if (kc >= p.K) continue;  // warp-uniform
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          sts128(my_row + c * 16, make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]));
+        __syncwarp();
+        // lane j: row 4 i + j / 8, 16-byte part j % 8
+        const int part = lane & 7;
+        const int32_t k = kc + part * 8;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int row = 4 * it + (lane >> 3);
+          const uint4 v = lds128_ordered(smem_addr(rows + row * kRowPitch + part * 16));
+          const int32_t nr = nbase + row;
+          if (nr < p.N && k < p.K)
+            *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t.g) * p.N + nr) * p.K + k) = v;
+        }
+        __syncwarp();  // staging rows free for the next step
+      }
+      if (!empty_group) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.acc_empty[b]);
+        ++tc;
+      }
     }
     tc_fence_before();
   }
