@@ -15,7 +15,8 @@
 // in a fixed order, each block every gridDim-th.  Warp roles:
 //   warp 0 (one lane): TMA loads of the tile's token chunks -- 128 tokens x
 //     128 n of qa_t and 2 x (128 tokens x 128 k) of qx, 48 KB, 128-byte
-//     swizzle -- into a ring of kStages stages;
+//     swizzle; a group's last chunk only as many 32-token slices as it
+//     needs -- into a ring of kStages stages;
 //   warp 1: allocates the 512 TMEM columns (two accumulators of 256 fp32
 //     columns, so that a tile's epilogue overlaps the next tile's MMAs);
 //     zeroes the token rows of a group's last chunk that lie past its end;
@@ -130,11 +131,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
                : "r"(taddr)
                : "memory");
 }
-// Keeps the registers of a TMEM load from being used before the wait that
-// precedes this point.
-__device__ __forceinline__ void tmem_pin(uint32_t (&r)[32]) {
-  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) : : "memory");
-}
 // Waits for this thread's TMEM loads; the registers pass through the asm so
 // that no use of them is scheduled before it.
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
@@ -176,9 +172,18 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | (1u << 16) |
                             (static_cast<uint32_t>(kBM >> 4) << 24);
 static_assert((kBN >> 3) < 64 && (kBM >> 4) < 32, "descriptor field widths");
 
+// Waits for the phase of `bar` with the given parity; bounded like
+// mbar_wait (records kErrMbarTimeout and returns false on expiry).
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                           unsigned* err) {
+  return mbar_wait(bar, parity, timeout_ns, err);
+}
+
 struct TileId {
   int32_t g, n0, k0, t0, tg;  // group, first row, first column, first token, tokens
 };
+
+constexpr int kScaleLoads = kBN / 32;  // sx values per lane and tile
 
 __device__ __forceinline__ TileId tile_of(const Params& p, const int32_t* ends, int64_t i) {
   const int64_t per_group = static_cast<int64_t>(p.tiles_n) * p.tiles_k;
@@ -192,9 +197,33 @@ __device__ __forceinline__ TileId tile_of(const Params& p, const int32_t* ends, 
   return t;
 }
 
+// The raw scales epilogue lane `lane` of quarter q needs for tile i: sx of
+// columns k0 + lane + 32 m and sa of row n0 + 32 q + lane (1 past the
+// ends, and for tiles past the last, so that the reciprocals stay finite).
+__device__ __forceinline__ void load_scales(const Params& p, const int32_t* ends, int64_t i, int q,
+                                            int lane, float (&x)[kScaleLoads], float& a) {
+  if (i >= p.tiles) {
+#pragma unroll
+    for (int m = 0; m < kScaleLoads; ++m) x[m] = 1.0f;
+    a = 1.0f;
+    return;
+  }
+  const TileId t = tile_of(p, ends, i);
+  const float* sxg = p.sx + static_cast<int64_t>(t.g) * p.K;
+#pragma unroll
+  for (int m = 0; m < kScaleLoads; ++m) {
+    const int32_t k = t.k0 + lane + 32 * m;
+    x[m] = k < p.K ? __ldg(sxg + k) : 1.0f;
+  }
+  const int32_t n = t.n0 + 32 * q + lane;
+  a = n < p.N ? __ldg(p.sa + static_cast<int64_t>(n) * p.G + t.g) : 1.0f;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     wgrad_kernel(const __grid_constant__ CUtensorMap amap,
-                 const __grid_constant__ CUtensorMap xmap, const Params p) {
+                 const __grid_constant__ CUtensorMap xmap,
+                 const __grid_constant__ CUtensorMap amap32,
+                 const __grid_constant__ CUtensorMap xmap32, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -217,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_mbar_init();
       prefetch_tensormap(&amap);
       prefetch_tensormap(&xmap);
+      prefetch_tensormap(&amap32);
+      prefetch_tensormap(&xmap32);
     }
   } else if (warp == 1) {
     tmem_alloc(&s.tmem_base, kTmemCols);
@@ -237,19 +268,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileId t = tile_of(p, s.ends, i);
         for (int32_t c = 0; ok && c < t.tg; c += kBK, ++it) {
           const int st = static_cast<int>(it % kStages);
-          ok = mbar_wait(&s.empty[st], ((it / kStages) & 1) ^ 1u, wait_ns, p.err);
+          ok = wait_phase(&s.empty[st], ((it / kStages) & 1) ^ 1u, wait_ns, p.err);
           if (!ok) break;
           uint8_t* base = s.stage[st];
-          mbar_arrive_expect_tx(&s.full[st], kStageBytes);
-          tma_load_2d(base + kBOff, &xmap, t.k0, t.t0 + c, &s.full[st], pol);
-          tma_load_2d(base + kBOff + kBHalfBytes, &xmap, t.k0 + kHalfN, t.t0 + c, &s.full[st],
-                      pol);
-          tma_load_2d(base + kAOff, &amap, t.n0, t.t0 + c, &s.full[st], pol);
+          const int32_t rem = min(t.tg - c, kBK);
+          if (rem == kBK) {
+            mbar_arrive_expect_tx(&s.full[st], kStageBytes);
+            tma_load_2d(base + kBOff, &xmap, t.k0, t.t0 + c, &s.full[st], pol);
+            tma_load_2d(base + kBOff + kBHalfBytes, &xmap, t.k0 + kHalfN, t.t0 + c, &s.full[st],
+                        pol);
+            tma_load_2d(base + kAOff, &amap, t.n0, t.t0 + c, &s.full[st], pol);
+          } else {
+            // a group's last, partial chunk: only the 32-token slices the
+            // MMAs will read
+            const int nsub = (rem + kSubK - 1) / kSubK;
+            mbar_arrive_expect_tx(&s.full[st], static_cast<uint32_t>(nsub * 3 * kSubK * 128));
+            for (int u = 0; u < nsub; ++u) {
+              const int32_t y = t.t0 + c + u * kSubK;
+              const int off = u * kSubK * 128;
+              tma_load_2d(base + kBOff + off, &xmap32, t.k0, y, &s.full[st], pol);
+              tma_load_2d(base + kBOff + kBHalfBytes + off, &xmap32, t.k0 + kHalfN, y, &s.full[st],
+                          pol);
+              tma_load_2d(base + kAOff + off, &amap32, t.n0, y, &s.full[st], pol);
+            }
+          }
         }
       }
       // the block must not exit while a load is still writing its memory
       for (uint32_t u = it > kStages ? it - kStages : 0; u < it; ++u)
-        mbar_wait(&s.full[u % kStages], (u / kStages) & 1, wait_ns, p.err);
+        wait_phase(&s.full[u % kStages], (u / kStages) & 1, wait_ns, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMAs --
@@ -260,13 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileId t = tile_of(p, s.ends, i);
       if (t.tg <= 0) continue;
       const int b = static_cast<int>(tc & 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(&s.acc_empty[b], ((tc >> 1) & 1) ^ 1u, wait_ns, p.err));
+      ok = __all_sync(0xffffffffu, wait_phase(&s.acc_empty[b], ((tc >> 1) & 1) ^ 1u, wait_ns, p.err));
       if (!ok) break;
       tc_fence_after();
       const uint32_t d = tmem + static_cast<uint32_t>(b * kAccCols);
       for (int32_t c = 0; c < t.tg; c += kBK, ++it) {
         const int st = static_cast<int>(it % kStages);
-        ok = __all_sync(0xffffffffu, mbar_wait(&s.full[st], (it / kStages) & 1, wait_ns, p.err));
+        ok = __all_sync(0xffffffffu, wait_phase(&s.full[st], (it / kStages) & 1, wait_ns, p.err));
         if (!ok) break;
         const int32_t rem = min(t.tg - c, kBK);  // tokens of the group in this chunk
         const int32_t used = (rem + kSubK - 1) / kSubK * kSubK;
@@ -308,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     issued = __shfl_sync(0xffffffffu, issued, 0);
     if (issued) {
       if (lane == 0) tc_commit(&s.drain);
-      mbar_wait(&s.drain, 0, wait_ns, p.err);
+      wait_phase(&s.drain, 0, wait_ns, p.err);
     }
   } else {
     // --------------------------------------------------------- epilogue --
@@ -323,58 +370,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* rx = s.rx[ew];
     uint8_t* rows = s.rows[ew];
     const uint32_t my_row = smem_addr(rows + lane * kRowPitch);
+    // The scales of a tile are loaded two tiles ahead: under the TMA traffic
+    // their latency is several microseconds, which would otherwise stall
+    // every tile's epilogue.
     uint32_t tc = 0;
     bool ok = true;
+    float x0[kScaleLoads], x1[kScaleLoads], x2[kScaleLoads];
+    float a0, a1, a2;
+    load_scales(p, s.ends, blockIdx.x, q, lane, x0, a0);
+    load_scales(p, s.ends, blockIdx.x + static_cast<int64_t>(gridDim.x), q, lane, x1, a1);
     for (int64_t i = blockIdx.x; ok && i < p.tiles; i += gridDim.x) {
+      load_scales(p, s.ends, i + 2 * static_cast<int64_t>(gridDim.x), q, lane, x2, a2);
       const TileId t = tile_of(p, s.ends, i);
       const int32_t nbase = t.n0 + 32 * q;
       const bool empty_group = t.tg <= 0;
-      // 1/sx of the tile's columns (0 past K)
-      const float* sxg = p.sx + static_cast<int64_t>(t.g) * p.K;
       __syncwarp();  // the previous tile's readers of rx are done
-      if (!empty_group)
-        for (int j = lane; j < kBN; j += 32)
-          rx[j] = t.k0 + j < p.K ? __frcp_rn(__ldg(sxg + t.k0 + j)) : 0.0f;
+      // 1/sx of the tile's columns (0 past K), 1/sa of this lane's row
+#pragma unroll
+      for (int m = 0; m < kScaleLoads; ++m)
+        rx[lane + 32 * m] = t.k0 + lane + 32 * m < p.K ? __frcp_rn(x0[m]) : 0.0f;
       const int32_t n = nbase + lane;
-      const float ra =
-          (!empty_group && n < p.N) ? __frcp_rn(__ldg(p.sa + static_cast<int64_t>(n) * p.G + t.g))
-                                    : 0.0f;
+      const float ra = n < p.N ? __frcp_rn(a0) : 0.0f;
+#pragma unroll
+      for (int m = 0; m < kScaleLoads; ++m) {
+        x0[m] = x1[m];
+        x1[m] = x2[m];
+      }
+      a0 = a1;
+      a1 = a2;
       const int b = static_cast<int>(tc & 1);
       if (!empty_group) {
         ok = __all_sync(0xffffffffu,
-                        mbar_wait(&s.acc_full[b], (tc >> 1) & 1, wait_ns, p.err));
+                        wait_phase(&s.acc_full[b], (tc >> 1) & 1, wait_ns, p.err));
         if (!ok) break;
         tc_fence_after();
       }
       __syncwarp();  // rx visible to the warp
+      // TMEM loads run one half-chunk (32 columns) ahead of the math:
+      // h0 / h1 hold columns [64 ch, 64 ch + 32) / [64 ch + 32, 64 ch + 64).
+      const uint32_t tacc = tmem + lane_base + static_cast<uint32_t>(b * kAccCols);
+      uint32_t h0[32], h1[32];
+      if (!empty_group) tmem_ld32(tacc, h0);
 #pragma unroll 1
       for (int ch = 0; ch < kBN / kChunk; ++ch) {
         const int32_t kc = t.k0 + ch * kChunk;
         uint32_t w[32];
         if (!empty_group) {
-          uint32_t r0[32], r1[32];
-          const uint32_t ta = tmem + lane_base + static_cast<uint32_t>(b * kAccCols + ch * kChunk);
-          tmem_ld32(ta, r0);
-          tmem_ld32(ta + 32, r1);
-          tmem_ld_wait(r0);
-          tmem_pin(r1);
           const float* rxc = rx + ch * kChunk;
+          tmem_ld_wait(h0);
+          tmem_ld32(tacc + static_cast<uint32_t>(ch * kChunk + 32), h1);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const __nv_bfloat162 h0 = __floats2bfloat162_rn(
-                __uint_as_float(r0[2 * e]) * ra * rxc[2 * e],
-                __uint_as_float(r0[2 * e + 1]) * ra * rxc[2 * e + 1]);
-            const __nv_bfloat162 h1 = __floats2bfloat162_rn(
-                __uint_as_float(r1[2 * e]) * ra * rxc[32 + 2 * e],
-                __uint_as_float(r1[2 * e + 1]) * ra * rxc[32 + 2 * e + 1]);
-            w[e] = *reinterpret_cast<const uint32_t*>(&h0);
-            w[16 + e] = *reinterpret_cast<const uint32_t*>(&h1);
+            const __nv_bfloat162 v = __floats2bfloat162_rn(
+                __uint_as_float(h0[2 * e]) * ra * rxc[2 * e],
+                __uint_as_float(h0[2 * e + 1]) * ra * rxc[2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&v);
+          }
+          tmem_ld_wait(h1);
+          if (ch + 1 < kBN / kChunk)
+            tmem_ld32(tacc + static_cast<uint32_t>((ch + 1) * kChunk), h0);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(
+                __uint_as_float(h1[2 * e]) * ra * rxc[32 + 2 * e],
+                __uint_as_float(h1[2 * e + 1]) * ra * rxc[32 + 2 * e + 1]);
+            w[16 + e] = *reinterpret_cast<const uint32_t*>(&v);
           }
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) w[e] = 0u;
         }
-        if (kc >= p.K) continue;  // warp-uniform
+        if (kc >= p.K) continue;  // warp-uniform; a load still in flight is waited for below
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           sts128(my_row + c * 16, make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]));
@@ -392,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();  // staging rows free for the next step
       }
+      if (!empty_group) tmem_ld_wait(h0);  // no TMEM load outlives the tile
       if (!empty_group) {
         tc_fence_before();
         __syncwarp();
@@ -419,15 +486,22 @@ gq_status setup(DeviceInfo& info) {
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* qa_t, const float* sa,
                  const void* qx, const float* sx, int32_t T, int32_t N, int32_t K,
                  const int32_t* offs, int32_t G, void* out, cudaStream_t stream) {
-  CUtensorMap amap, xmap;
-  gq_status st = encode_tiled_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(qa_t),
-                                 static_cast<uint64_t>(N), static_cast<uint64_t>(T),
-                                 static_cast<uint64_t>(N), kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != GQ_OK) return st;
-  st = encode_tiled_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(qx),
-                       static_cast<uint64_t>(K), static_cast<uint64_t>(T),
-                       static_cast<uint64_t>(K), kHalfN, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != GQ_OK) return st;
+  // 128-token boxes for full chunks, 32-token boxes for a group's last one
+  CUtensorMap amap, xmap, amap32, xmap32;
+  const struct {
+    CUtensorMap* map;
+    const void* base;
+    int32_t inner;
+    uint32_t rows;
+  } maps[4] = {{&amap, qa_t, N, kBK}, {&xmap, qx, K, kBK}, {&amap32, qa_t, N, kSubK},
+               {&xmap32, qx, K, kSubK}};
+  for (const auto& m : maps) {
+    const gq_status st = encode_tiled_2d(m.map, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                         const_cast<void*>(m.base), static_cast<uint64_t>(m.inner),
+                                         static_cast<uint64_t>(T), static_cast<uint64_t>(m.inner),
+                                         128, m.rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != GQ_OK) return st;
+  }
   Params p;
   p.sa = sa;
   p.sx = sx;
@@ -443,7 +517,8 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* qa_t
   p.tiles = static_cast<int64_t>(p.tiles_n) * p.tiles_k * G;
   p.timeout_ns = dbg.timeout_ns;
   const int64_t grid = p.tiles < info.sm_count ? p.tiles : info.sm_count;
-  wgrad_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, stream>>>(amap, xmap, p);
+  wgrad_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, stream>>>(amap, xmap, amap32, xmap32,
+                                                                         p);
   return check_cuda(cudaGetLastError(), "grouped_wgrad: launch");
 }
 
