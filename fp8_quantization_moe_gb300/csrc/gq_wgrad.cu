@@ -85,6 +85,7 @@ struct Params {
   int32_t tiles_n, tiles_k;
   int64_t tiles;
   uint64_t timeout_ns;
+  int32_t skip_arrival;  // test hook: block 0 never frees its first accumulator
 };
 
 // ------------------------------------------------------------ tcgen05 --
@@ -462,7 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!empty_group) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.acc_empty[b]);
+        if (lane == 0 && !(p.skip_arrival && blockIdx.x == 0 && tc == 0))
+          mbar_arrive(&s.acc_empty[b]);
         ++tc;
       }
     }
@@ -516,6 +518,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* qa_t
   p.tiles_k = (K + kBN - 1) / kBN;
   p.tiles = static_cast<int64_t>(p.tiles_n) * p.tiles_k * G;
   p.timeout_ns = dbg.timeout_ns;
+  p.skip_arrival = dbg.skip_arrival;
   const int64_t grid = p.tiles < info.sm_count ? p.tiles : info.sm_count;
   wgrad_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, stream>>>(amap, xmap, amap32, xmap32,
                                                                          p);

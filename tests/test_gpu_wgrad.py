@@ -116,3 +116,38 @@ def test_grouped_wgrad_full_size_sampled(gq):
                                        np.ascontiguousarray(case.sx[:, ks]), case.offs)
     worst = check(got, want, absum, case.name)
     print(f"{case.name} sampled: max |err| / S = {worst:.3g}")
+
+
+def test_grouped_wgrad_out_of_contract_offsets(gq):
+    """Decreasing and out-of-range end offsets are read as the running
+    maximum clamped to [0, T], as in the quantization calls."""
+    T, N, K = 200, 128, 256
+    offs = np.array([60, 40, 150, 500], np.int32)   # -> ends 60, 60, 150, 200
+    case = synth.wgrad_case(T, N, K, offs, seed=905)
+    got = run_gpu(gq, case)
+    want, absum = oracle.grouped_wgrad(case.qa_t, case.sa, case.qx, case.sx, case.offs)
+    check(got, want, absum, "out-of-contract offsets")
+    assert not got[1].any()
+
+
+def test_grouped_wgrad_timeout_is_reported_not_hung(gq):
+    """A withheld accumulator release makes block 0's MMA warp give up after
+    the (shortened) limit; every role leaves its loop, the TMEM is freed and
+    the call reports GQ_ERR_TIMEOUT; the next call is fine."""
+    T, N, K = 256, 1024, 2048          # 8 x 8 tiles per group: block 0 gets 4 tiles
+    offs = np.arange(32, T + 1, 32, dtype=np.int32)
+    case = synth.wgrad_case(T, N, K, offs, seed=906)
+    try:
+        gq.debug_set(skip_arrival=True, wait_timeout_ns=5_000_000)
+        dev = torch.device("cuda")
+        gq.grouped_wgrad(torch.from_numpy(case.qa_t).to(dev), torch.from_numpy(case.sa).to(dev),
+                         torch.from_numpy(case.qx).to(dev), torch.from_numpy(case.sx).to(dev),
+                         torch.from_numpy(case.offs).to(dev))
+        with pytest.raises(gq.GQError) as e:
+            gq.check_device_error()
+        assert e.value.status == 4
+    finally:
+        gq.debug_set(False, 0)
+    got = run_gpu(gq, case)
+    want, absum = oracle.grouped_wgrad(case.qa_t, case.sa, case.qx, case.sx, case.offs)
+    check(got, want, absum, "after a timeout")
