@@ -24,6 +24,7 @@ GQ_KIND_COLWISE = 0
 GQ_KIND_ROWWISE_T = 1
 GQ_MAX_GROUPS = 1024
 GQ_SCALE_POW2 = 1
+GQ_WORKSPACE_ZEROED = 2
 GQ_MX_FLOOR = 0
 GQ_MX_RCEIL = 1
 
@@ -110,16 +111,20 @@ _ws_cache: dict = {}
 _ws_lock = threading.Lock()
 
 
-def _workspace(nbytes: int, device: torch.device, stream_handle: int):
-    """A cached device workspace per (device, stream); the library clears it
-    on every call, so reuse across calls on one stream is safe."""
+def _workspace(nbytes: int, device: torch.device, stream_handle: int, kind: int = 0):
+    """A cached device workspace per (device, stream, kind), zero-filled when
+    it is allocated.  Calls on one stream run in order, so reuse is safe: the
+    library clears what it uses on every call, except rowwise_t given
+    GQ_WORKSPACE_ZEROED, whose kernel leaves its counters at zero when it
+    ends (its cache is used by rowwise_t alone)."""
     if nbytes == 0:
         return None
-    key = (device.index, stream_handle)
+    key = (device.index, stream_handle, kind)
     with _ws_lock:
         buf = _ws_cache.get(key)
         if buf is None or buf.numel() < nbytes:
-            buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+            buf = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
+            torch.cuda.synchronize(device)  # zero before work on any stream uses it
             _ws_cache[key] = buf
     return buf
 
@@ -215,12 +220,18 @@ def rowwise_t(a: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
         raise ValueError("rowwise_t: scales must be a contiguous float32 (N, G) tensor")
     sh = _stream_handle(stream, dev)
     need = workspace_bytes(GQ_KIND_ROWWISE_T, N, Mg, G)
-    ws = workspace if workspace is not None else _workspace(need, dev, sh)
+    flags = GQ_SCALE_POW2 if pow2_scales else 0
+    if workspace is None:
+        # the cache is zero-filled and only rowwise_t uses it: its counters
+        # are zero whenever a call starts
+        ws = _workspace(need, dev, sh, GQ_KIND_ROWWISE_T)
+        flags |= GQ_WORKSPACE_ZEROED if ws is not None else 0
+    else:
+        ws = workspace
     wp, wn = _ws_ptr(ws)
     with torch.cuda.device(dev):
         st = lib().gq_fp8_rowwise_t_ex(_ptr(a), N, Mg, _ptr(offs), G, _ptr(out),
-                                       _ptr(scales), GQ_SCALE_POW2 if pow2_scales else 0,
-                                       wp, wn, sh)
+                                       _ptr(scales), flags, wp, wn, sh)
     _check(st, "gq_fp8_rowwise_t")
     return out, scales
 

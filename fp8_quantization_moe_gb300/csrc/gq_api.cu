@@ -189,7 +189,8 @@ using namespace gq;
 
 namespace {
 
-constexpr uint32_t kKnownFlags = GQ_SCALE_POW2;
+constexpr uint32_t kKnownFlags = GQ_SCALE_POW2;  // every call
+constexpr uint32_t kRowwiseFlags = GQ_SCALE_POW2 | GQ_WORKSPACE_ZEROED;
 
 gq_status validate_common(const void* in, const void* out, const int32_t* offs,
                           int32_t n_groups, const float* scales, int64_t rows,
@@ -341,8 +342,8 @@ gq_status gq_fp8_rowwise_t_ex(const void* a, int64_t N, int64_t Mg,
                               float* scales, uint32_t flags, void* workspace,
                               size_t workspace_bytes, gq_stream_t stream) {
   const char* name = "gq_fp8_rowwise_t";
-  if (flags & ~kKnownFlags)
-    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kKnownFlags);
+  if (flags & ~kRowwiseFlags)
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kRowwiseFlags);
   gq_status st = validate_common(a, out_t, offs, n_groups, scales, N, Mg, name);
   if (st != GQ_OK) return st;
   if (N % 16 != 0)

@@ -68,7 +68,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
 namespace rowwise {
 constexpr int kTn = 64;  // rows of A per window: one row band
 constexpr int kTm = 64;  // token columns per window
-constexpr size_t kWorkspaceBytes = 256;  // the unit counter, padded
+constexpr size_t kWorkspaceBytes = 256;  // unit counter, finished-blocks counter, padded
 gq_status setup(DeviceInfo& info);
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
                  int32_t N, int32_t Mg, const int32_t* offs, int32_t G,

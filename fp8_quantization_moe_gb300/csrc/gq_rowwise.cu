@@ -111,7 +111,7 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
 struct Params {
   const int32_t* offs;
-  uint32_t* ticket;  // unit counter
+  uint32_t* ticket;  // unit counter; ticket[1]: blocks finished
   uint8_t* out_t;
   float* scales;
   unsigned* err;
@@ -516,6 +516,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     loader_warp(s, &amap, p, lane);
   else
     consumer_warp(s, p, warp, lane);
+
+  // The last block to finish returns the counters to zero, so that the next
+  // call on this workspace may skip its clear (GQ_WORKSPACE_ZEROED).  Every
+  // block gets here, also after a bounded wait expired, and has made its
+  // last claim before its arrival is counted.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.ticket + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.ticket, 0u);
+      atomicExch(p.ticket + 1, 0u);
+    }
+  }
 }
 
 // ---------------------------------------------------------------- host --
@@ -569,8 +582,10 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
   p.skip_arrival = dbg.skip_arrival;
   p.pow2 = (flags & GQ_SCALE_POW2) != 0;
 
-  st = check_cuda(cudaMemsetAsync(ws, 0, 4, stream), "rowwise_t: clear unit counter");
-  if (st != GQ_OK) return st;
+  if (!(flags & GQ_WORKSPACE_ZEROED)) {
+    st = check_cuda(cudaMemsetAsync(ws, 0, 8, stream), "rowwise_t: clear the counters");
+    if (st != GQ_OK) return st;
+  }
   rowwise_kernel<<<grid, kThreads, kSmemBytes, stream>>>(amap, p);
   return check_cuda(cudaGetLastError(), "rowwise_t: launch");
 }

@@ -80,10 +80,11 @@ typedef enum gq_status {
  *   kind GQ_KIND_ROWWISE_T: rows = N, cols = Mg.
  * Colwise: a work counter, one completion counter per column slab (128
  * columns) and the per-(group, column) running amax words.  Rowwise_t: a
- * work counter only (256 bytes), since each (row band, group) pair is
- * finished by one thread block.  The call clears what it uses itself, so
- * the contents on entry do not matter.  Returns 0 when no workspace is
- * needed (empty problems) and for invalid arguments.
+ * work counter and a finished-blocks counter (256 bytes), since each (row
+ * band, group) pair is finished by one thread block.  The call clears what
+ * it uses itself, so the contents on entry do not matter (rowwise_t with
+ * GQ_WORKSPACE_ZEROED skips the clear; see there).  Returns 0 when no
+ * workspace is needed (empty problems) and for invalid arguments.
  */
 size_t gq_workspace_bytes(int kind, int64_t rows, int64_t cols,
                           int32_t n_groups);
@@ -146,6 +147,16 @@ gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,
  *                  least 1e-12 the largest |q| lies in [224, 448].
  */
 #define GQ_SCALE_POW2 1u
+/*
+ *   GQ_WORKSPACE_ZEROED  (gq_fp8_rowwise_t_ex only; GQ_ERR_INVALID_ARG
+ *                  elsewhere) the caller states that the first 8 bytes of
+ *                  the workspace are zero -- zero-filled once, or left so by
+ *                  an earlier rowwise_t call that completed: every rowwise_t
+ *                  launch returns its counters to zero before it ends, also
+ *                  after a bounded wait expired -- and the call skips its own
+ *                  clear of them (one device operation less per call).
+ */
+#define GQ_WORKSPACE_ZEROED 2u
 
 /*
  * gq_fp8_colwise / gq_fp8_rowwise_t with option flags; the calls above are

@@ -418,3 +418,27 @@ def test_mxfp8_dim0(gq, M, K, mode):
     gq_q, gq_s = q.view(torch.uint8).cpu().numpy(), s.cpu().numpy()
     assert np.array_equal(gq_s, rs), f"{mode} scales: {np.argwhere(gq_s != rs)[:3]}"
     assert np.array_equal(gq_q, rq), f"{mode} codes: {np.argwhere(gq_q != rq)[:3]}"
+
+
+def test_rowwise_workspace_left_zeroed(gq):
+    """Every rowwise_t launch returns its counters to zero, so calls given
+    GQ_WORKSPACE_ZEROED on one workspace (zero-filled once) stay exact --
+    across shapes and group counts, and after a call without the flag."""
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    cases = [synth.random_case("rowwise_t", 144, 520, 6, seed=70, n_empty=1, scale_mix=True),
+             synth.random_case("rowwise_t", 1040, 3000, 9, seed=71, n_empty=1, align=1, uncovered=3),
+             synth.random_case("rowwise_t", 64, 16, 1, seed=72)]
+    for rep in range(2):
+        for c in cases:
+            a, o = dev_bf16(c.x), dev_i32(c.offs)
+            qt = torch.full((c.x.shape[1], c.x.shape[0]), SENTINEL, dtype=torch.uint8, device="cuda")
+            s = torch.empty((c.x.shape[0], len(c.offs)), dtype=torch.float32, device="cuda")
+            st = gq.lib().gq_fp8_rowwise_t_ex(
+                a.data_ptr(), c.x.shape[0], c.x.shape[1], o.data_ptr(), len(c.offs),
+                qt.data_ptr(), s.data_ptr(), gq.GQ_WORKSPACE_ZEROED if rep == 0 else 0,
+                ws.data_ptr(), 256, torch.cuda.current_stream().cuda_stream)
+            assert st == 0
+            gq.check_device_error()
+            assert not ws[:8].any().item(), "counters not returned to zero"
+            rq, rs = oracle.rowwise_t(c.x, c.offs, out=np.full((c.x.shape[1], c.x.shape[0]), SENTINEL, np.uint8))
+            assert_same(qt.cpu().numpy(), s.cpu().numpy(), rq, rs, c.name)

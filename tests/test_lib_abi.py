@@ -59,8 +59,7 @@ def test_workspace_bytes(gq):
     # colwise 65536x4096, 16 groups: 256 B header + 32 slab counters (256 B)
     # + 16*4096 amax words
     assert gq.workspace_bytes(0, 65536, 4096, 16) == 256 + 256 + 16 * 4096 * 4
-    # rowwise_t 8192x16640, 64 groups: 128 band counters (512 B) + 8192*64
-    # amax words
+    # rowwise_t: a unit counter and a finished-blocks counter, padded
     assert gq.workspace_bytes(1, 8192, 16640, 64) == 256
     assert gq.workspace_bytes(0, 0, 4096, 4) == 0
     assert gq.workspace_bytes(1, 16, 0, 4) == 0
@@ -139,8 +138,10 @@ def test_ex_calls_reject_unknown_flags(gq):
     """The _ex calls check their flags before anything else (no GPU needed)."""
     lib = gq.lib()
     assert gq.GQ_SCALE_POW2 == 1
-    for bad in (2, 0x80000000, 3):
+    assert gq.GQ_WORKSPACE_ZEROED == 2
+    for bad in (2, 0x80000000, 3):   # GQ_WORKSPACE_ZEROED is rowwise_t's alone
         assert lib.gq_fp8_colwise_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1
+    for bad in (4, 0x80000000, 7):
         assert lib.gq_fp8_rowwise_t_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1
 
 
