@@ -112,21 +112,26 @@ _ws_lock = threading.Lock()
 
 
 def _workspace(nbytes: int, device: torch.device, stream_handle: int, kind: int = 0):
-    """A cached device workspace per (device, stream, kind), zero-filled when
-    it is allocated.  Calls on one stream run in order, so reuse is safe: the
-    library clears what it uses on every call, except rowwise_t given
-    GQ_WORKSPACE_ZEROED, whose kernel leaves its counters at zero when it
-    ends (its cache is used by rowwise_t alone)."""
+    """(buffer, zeroed): a cached device workspace per (device, stream, kind),
+    zero-filled when it is allocated.  Calls on one stream run in order, so
+    reuse is safe: the library clears what it uses on every call, except
+    rowwise_t given GQ_WORKSPACE_ZEROED, whose kernel leaves its counters at
+    zero when it ends (its cache is used by rowwise_t alone).  While the
+    stream is being captured into a CUDA graph a missing buffer is not
+    created in the cache (that would synchronise the device): the call gets
+    a fresh one, not known to be zero."""
     if nbytes == 0:
-        return None
+        return None, False
     key = (device.index, stream_handle, kind)
     with _ws_lock:
         buf = _ws_cache.get(key)
         if buf is None or buf.numel() < nbytes:
+            if torch.cuda.is_current_stream_capturing():
+                return torch.empty(nbytes + 256, dtype=torch.uint8, device=device), False
             buf = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
             torch.cuda.synchronize(device)  # zero before work on any stream uses it
             _ws_cache[key] = buf
-    return buf
+    return buf, True
 
 
 def _ptr(t):
@@ -187,7 +192,7 @@ def colwise(x: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
         raise ValueError("colwise: scales must be a contiguous float32 (G, K) tensor")
     sh = _stream_handle(stream, dev)
     need = workspace_bytes(GQ_KIND_COLWISE, M, K, G)
-    ws = workspace if workspace is not None else _workspace(need, dev, sh)
+    ws = workspace if workspace is not None else _workspace(need, dev, sh)[0]
     wp, wn = _ws_ptr(ws)
     with torch.cuda.device(dev):
         st = lib().gq_fp8_colwise_ex(_ptr(x), M, K, _ptr(offs), G, _ptr(out),
@@ -224,8 +229,8 @@ def rowwise_t(a: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
     if workspace is None:
         # the cache is zero-filled and only rowwise_t uses it: its counters
         # are zero whenever a call starts
-        ws = _workspace(need, dev, sh, GQ_KIND_ROWWISE_T)
-        flags |= GQ_WORKSPACE_ZEROED if ws is not None else 0
+        ws, zeroed = _workspace(need, dev, sh, GQ_KIND_ROWWISE_T)
+        flags |= GQ_WORKSPACE_ZEROED if zeroed else 0
     else:
         ws = workspace
     wp, wn = _ws_ptr(ws)
@@ -256,7 +261,7 @@ def expert_dim1(w: torch.Tensor, *, out=None, scales=None, stream=None, workspac
         raise ValueError("expert_dim1: scales must be a contiguous float32 (E, N) tensor")
     sh = _stream_handle(stream, dev)
     need = workspace_bytes(GQ_KIND_COLWISE, E * K, N, E)
-    ws = workspace if workspace is not None else _workspace(need, dev, sh)
+    ws = workspace if workspace is not None else _workspace(need, dev, sh)[0]
     wp, wn = _ws_ptr(ws)
     with torch.cuda.device(dev):
         st = lib().gq_fp8_expert_dim1(_ptr(w), E, K, N, _ptr(out), _ptr(scales),

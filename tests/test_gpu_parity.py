@@ -442,3 +442,32 @@ def test_rowwise_workspace_left_zeroed(gq):
             assert not ws[:8].any().item(), "counters not returned to zero"
             rq, rs = oracle.rowwise_t(c.x, c.offs, out=np.full((c.x.shape[1], c.x.shape[0]), SENTINEL, np.uint8))
             assert_same(qt.cpu().numpy(), s.cpu().numpy(), rq, rs, c.name)
+
+
+def test_graph_capture_and_replay(gq):
+    """Both calls captured into one CUDA graph on a fresh stream (so the
+    workspaces are created during the capture) and replayed: each replay
+    gives the oracle's bytes."""
+    c = synth.random_case("colwise", 700, 272, 5, seed=81, n_empty=1, align=1, scale_mix=True)
+    r = synth.random_case("rowwise_t", 144, 520, 6, seed=82, n_empty=1, scale_mix=True)
+    x, xo, a, ao = dev_bf16(c.x), dev_i32(c.offs), dev_bf16(r.x), dev_i32(r.offs)
+    q = torch.full(c.x.shape, SENTINEL, dtype=torch.uint8, device="cuda")
+    qs = torch.empty((len(c.offs), c.x.shape[1]), dtype=torch.float32, device="cuda")
+    qt = torch.full(r.x.shape[::-1], SENTINEL, dtype=torch.uint8, device="cuda")
+    ts = torch.empty((r.x.shape[0], len(r.offs)), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        gq.colwise(x, xo, out=q.view(torch.float8_e4m3fn), scales=qs, stream=s)
+        gq.rowwise_t(a, ao, out=qt.view(torch.float8_e4m3fn), scales=ts, stream=s)
+    rq, rs = oracle.colwise(c.x, c.offs, out=np.full(c.x.shape, SENTINEL, np.uint8))
+    tq, trs = oracle.rowwise_t(r.x, r.offs, out=np.full(r.x.shape[::-1], SENTINEL, np.uint8))
+    for _ in range(2):
+        q.fill_(SENTINEL)
+        qt.fill_(SENTINEL)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        gq.check_device_error()
+        assert_same(q.cpu().numpy(), qs.cpu().numpy(), rq, rs, "colwise in a graph")
+        assert_same(qt.cpu().numpy(), ts.cpu().numpy(), tq, trs, "rowwise_t in a graph")
