@@ -189,3 +189,20 @@ def test_mxfp8_host_validation(gq, args, status):
 ])
 def test_grouped_wgrad_host_validation(gq, args, status):
     assert gq.lib().gq_grouped_wgrad(*args, None) == status
+
+
+def test_header_compiles_as_c(tmp_path):
+    """The boundary is a C ABI: the header compiles as strict C99 (and C++)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "use.c"
+    src.write_text('#include "gq_fp8.h"\n'
+                   "int main(void) { return (int)gq_workspace_bytes(GQ_KIND_ROWWISE_T, 64, 64, 1) & 0; }\n")
+    inc = os.path.dirname(HEADER)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc,
+                    "-fsyntax-only", str(src)], check=True)
+    if shutil.which("g++") is not None:
+        subprocess.run(["g++", "-std=c++17", "-Wall", "-Wextra", "-Werror", "-I", inc,
+                        "-fsyntax-only", "-x", "c++", str(src)], check=True)
