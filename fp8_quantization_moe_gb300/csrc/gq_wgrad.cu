@@ -25,12 +25,14 @@
 //     the operands are contiguous along n and k) and commits each stage back
 //     to the producer and each finished accumulator to the epilogue;
 //   warps 2-5: each reads its 32 TMEM lanes (rows n) with tcgen05.ld, 64
-//     columns at a time, scales, rounds to bf16, stages the 32 rows' 128-byte
-//     runs in shared memory and stores them as whole lines.
+//     columns at a time, scales (the scales of a tile are loaded two tiles
+//     ahead), rounds to bf16, stages the 32 rows' 128-byte runs in shared
+//     memory and stores them as whole lines.
 // A group with no tokens gets zeros from the epilogue without any MMA.
 // Every wait is bounded; on expiry the error word is set, the warp leaves
-// its loop (as a whole: the lanes agree through __all_sync), the others time out in turn, loads and MMAs still in flight are
-// waited for, and the TMEM is freed before the block exits.
+// its loop (as a whole: the lanes agree through __all_sync), the others
+// time out in turn, loads and MMAs still in flight are waited for, and the
+// TMEM is freed before the block exits.
 #include <cuda_bf16.h>
 
 #include "gq_device.cuh"
@@ -51,6 +53,7 @@ constexpr int kStageBytes = kABytes + 2 * kBHalfBytes;
 // Stage layout: the two qx boxes (k 0-127, k 128-255), then the qa_t box.
 constexpr int kBOff = 0;
 constexpr int kAOff = 2 * kBHalfBytes;
+static_assert(kABytes == kBHalfBytes, "three operand blocks of 16 KB, back to back");
 constexpr int kAccCols = kBN;              // fp32 TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kEpiWarps = 4;
@@ -173,13 +176,6 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 15) | (1u << 16) |
                             (static_cast<uint32_t>(kBM >> 4) << 24);
 static_assert((kBN >> 3) < 64 && (kBM >> 4) < 32, "descriptor field widths");
 
-// Waits for the phase of `bar` with the given parity; bounded like
-// mbar_wait (records kErrMbarTimeout and returns false on expiry).
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
-                                           unsigned* err) {
-  return mbar_wait(bar, parity, timeout_ns, err);
-}
-
 struct TileId {
   int32_t g, n0, k0, t0, tg;  // group, first row, first column, first token, tokens
 };
@@ -199,8 +195,9 @@ __device__ __forceinline__ TileId tile_of(const Params& p, const int32_t* ends, 
 }
 
 // The raw scales epilogue lane `lane` of quarter q needs for tile i: sx of
-// columns k0 + lane + 32 m and sa of row n0 + 32 q + lane (1 past the
-// ends, and for tiles past the last, so that the reciprocals stay finite).
+// columns k0 + lane + 32 m and sa of row n0 + 32 q + lane; 1.0 for columns
+// past K, rows past N and tiles past the last, so that every reciprocal
+// stays finite.
 __device__ __forceinline__ void load_scales(const Params& p, const int32_t* ends, int64_t i, int q,
                                             int lane, float (&x)[kScaleLoads], float& a) {
   if (i >= p.tiles) {
@@ -269,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileId t = tile_of(p, s.ends, i);
         for (int32_t c = 0; ok && c < t.tg; c += kBK, ++it) {
           const int st = static_cast<int>(it % kStages);
-          ok = wait_phase(&s.empty[st], ((it / kStages) & 1) ^ 1u, wait_ns, p.err);
+          ok = mbar_wait(&s.empty[st], ((it / kStages) & 1) ^ 1u, wait_ns, p.err);
           if (!ok) break;
           uint8_t* base = s.stage[st];
           const int32_t rem = min(t.tg - c, kBK);
@@ -297,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // the block must not exit while a load is still writing its memory
       for (uint32_t u = it > kStages ? it - kStages : 0; u < it; ++u)
-        wait_phase(&s.full[u % kStages], (u / kStages) & 1, wait_ns, p.err);
+        mbar_wait(&s.full[u % kStages], (u / kStages) & 1, wait_ns, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMAs --
@@ -308,13 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileId t = tile_of(p, s.ends, i);
       if (t.tg <= 0) continue;
       const int b = static_cast<int>(tc & 1);
-      ok = __all_sync(0xffffffffu, wait_phase(&s.acc_empty[b], ((tc >> 1) & 1) ^ 1u, wait_ns, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s.acc_empty[b], ((tc >> 1) & 1) ^ 1u, wait_ns, p.err));
       if (!ok) break;
       tc_fence_after();
       const uint32_t d = tmem + static_cast<uint32_t>(b * kAccCols);
       for (int32_t c = 0; c < t.tg; c += kBK, ++it) {
         const int st = static_cast<int>(it % kStages);
-        ok = __all_sync(0xffffffffu, wait_phase(&s.full[st], (it / kStages) & 1, wait_ns, p.err));
+        ok = __all_sync(0xffffffffu, mbar_wait(&s.full[st], (it / kStages) & 1, wait_ns, p.err));
         if (!ok) break;
         const int32_t rem = min(t.tg - c, kBK);  // tokens of the group in this chunk
         const int32_t used = (rem + kSubK - 1) / kSubK * kSubK;
@@ -325,8 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // one swizzle row, so the swizzle does not matter)
           const int n16 = (used - rem) * 8;
           for (int j = lane; j < 3 * n16; j += 32) {
-            const int blk = j / n16, w = j % n16;
-            const uint32_t off = static_cast<uint32_t>(blk * kABytes + rem * 128 + w * 16);
+            const int blk = j / n16, w = j % n16;  // block 0, 1: qx halves; 2: qa_t
+            const uint32_t off = static_cast<uint32_t>(blk * kBHalfBytes + rem * 128 + w * 16);
             sts128(smem_addr(base + off), make_uint4(0u, 0u, 0u, 0u));
           }
           fence_proxy_async_smem();
@@ -356,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     issued = __shfl_sync(0xffffffffu, issued, 0);
     if (issued) {
       if (lane == 0) tc_commit(&s.drain);
-      wait_phase(&s.drain, 0, wait_ns, p.err);
+      mbar_wait(&s.drain, 0, wait_ns, p.err);
     }
   } else {
     // --------------------------------------------------------- epilogue --
@@ -402,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = static_cast<int>(tc & 1);
       if (!empty_group) {
         ok = __all_sync(0xffffffffu,
-                        wait_phase(&s.acc_full[b], (tc >> 1) & 1, wait_ns, p.err));
+                        mbar_wait(&s.acc_full[b], (tc >> 1) & 1, wait_ns, p.err));
         if (!ok) break;
         tc_fence_after();
       }
