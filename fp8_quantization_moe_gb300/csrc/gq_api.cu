@@ -466,7 +466,7 @@ const char* gq_status_string(gq_status status) {
 
 const char* gq_last_error(void) { return g_msg; }
 
-int gq_version(void) { return 100; }
+int gq_version(void) { return 200; }  // 0.2.0: mxfp8_dim0, grouped_wgrad, GQ_WORKSPACE_ZEROED
 
 gq_status gq_set_lag(int kind, int32_t lag) {
   if (kind != GQ_KIND_COLWISE && kind != GQ_KIND_ROWWISE_T)

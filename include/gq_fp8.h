@@ -301,8 +301,10 @@ int gq_version(void);
  * colwise: the first phase-A tile of the first column slab, whose waiters
  * are other thread blocks; rowwise_t: the amax-complete signal of the
  * (first row band, first group) unit, whose waiters are the warps that
- * would cast it -- so that the waiters must time out and report
- * GQ_ERR_TIMEOUT.  Process-wide; not thread-safe with concurrent calls.
+ * would cast it; grouped_wgrad: the release of thread block 0's first TMEM
+ * accumulator, whose waiter is the block's MMA warp -- so that the waiters
+ * must time out and report GQ_ERR_TIMEOUT.  Process-wide; not thread-safe
+ * with concurrent calls.
  */
 gq_status gq_debug_set(int skip_arrival, int64_t wait_timeout_ns);
 
