@@ -50,7 +50,9 @@ PAGES_CONTEXT = {
     "source": "pytorch/ao #2668 new-autotune table; #2863 Benchmarks table",
 }
 POW2 = False  # --pow2-scales
-KERNEL_SOURCES = ["gq_device.cuh", "gq_colwise.cu", "gq_rowwise.cu"]
+# the sources each kernel's recorded DRAM traffic depends on
+KERNEL_SOURCES = {"colwise": ["gq_device.cuh", "gq_colwise.cu"],
+                  "rowwise_t": ["gq_device.cuh", "gq_rowwise.cu"]}
 
 
 # ------------------------------------------------------------- helpers --
@@ -67,10 +69,10 @@ def step_bytes():
     return colwise_bytes(*COLWISE_SHAPE) + rowwise_bytes(*ROWWISE_SHAPE)
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "fp8_quantization_moe_gb300", "csrc")
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -96,7 +98,7 @@ def traffic_record(kernel: str):
     except (OSError, ValueError):
         return None
     rec = d.get(kernel)
-    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
+    if not rec or rec.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     return rec
 
