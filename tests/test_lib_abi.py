@@ -206,3 +206,17 @@ def test_header_compiles_as_c(tmp_path):
     if shutil.which("g++") is not None:
         subprocess.run(["g++", "-std=c++17", "-Wall", "-Wextra", "-Werror", "-I", inc,
                         "-fsyntax-only", "-x", "c++", str(src)], check=True)
+
+
+def test_binding_rejects_bad_wgrad_and_mxfp8_args(gq):
+    """The binding checks shapes, dtypes and devices on the host (no GPU)."""
+    import torch
+    f8 = torch.zeros((32, 16), dtype=torch.uint8)
+    s = torch.zeros((16, 2), dtype=torch.float32)
+    o = torch.tensor([16, 32], dtype=torch.int32)
+    with pytest.raises(ValueError):   # host tensors
+        gq.grouped_wgrad(f8, s, f8, torch.zeros((2, 16)), o)
+    with pytest.raises(ValueError):   # host tensors
+        gq.mxfp8_dim0(torch.zeros((4, 32), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):   # unknown mode is checked before the device
+        gq.mxfp8_dim0(torch.zeros((4, 32), dtype=torch.bfloat16), "nearest")
