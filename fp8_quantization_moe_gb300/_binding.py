@@ -383,18 +383,41 @@ def set_lag(kind: int, lag: int = 0):
 
 # ------------------------------------------------------ host-buffer calls --
 
-def _to_device(t, device, name):
+_h2d_streams: dict = {}  # (device, stream) -> side stream for host->device copies
+
+
+def _to_device(t, device, s, name):
+    """Copies a host tensor to the device on a side stream, so that the copy
+    can run while the work already queued on ``s`` (the previous call's
+    kernel and device->host copies) finishes; ``s`` waits for the copy.  The
+    device buffer is allocated on the side stream and recorded on ``s``, so
+    the allocator reuses it only after the side stream's copy and ``s``'s use
+    of it are both done."""
     if t.is_cuda:
         raise ValueError(f"{name}: expected a host tensor")
-    return t.to(device, non_blocking=True)
+    key = (device.index, s.cuda_stream)
+    with _ws_lock:
+        cs = _h2d_streams.get(key)
+        if cs is None:
+            cs = torch.cuda.Stream(device)
+            _h2d_streams[key] = cs
+    with torch.cuda.stream(cs):
+        d = t.to(device, non_blocking=True)
+    ev = torch.cuda.Event()
+    ev.record(cs)
+    s.wait_event(ev)
+    d.record_stream(s)
+    return d
 
 
 def colwise_host(x_host, offs_host, out_host=None, scales_host=None, *,
                  device="cuda", stream=None, pow2_scales: bool = False):
     """End-to-end colwise call on host buffers: host->device copies of x and
-    offs, the kernel, device->host copies of q and scales, all enqueued on
-    ``stream``.  Pinned host tensors make the copies asynchronous; the caller
-    synchronises before reading the results."""
+    offs (on a side stream that ``stream`` waits for, so that they overlap
+    the work already queued), the kernel and the device->host copies of q
+    and scales on ``stream``.  Pinned host tensors make the copies
+    asynchronous; the caller synchronises ``stream`` before reading the
+    results and keeps the host inputs unchanged until then."""
     dev = torch.device(device)
     M, K = x_host.shape
     G = offs_host.numel()
@@ -403,9 +426,9 @@ def colwise_host(x_host, offs_host, out_host=None, scales_host=None, *,
     if scales_host is None:
         scales_host = torch.empty((G, K), dtype=torch.float32, pin_memory=True)
     s = torch.cuda.current_stream(dev) if stream is None else stream
+    x = _to_device(x_host, dev, s, "colwise_host")
+    o = _to_device(offs_host, dev, s, "colwise_host")
     with torch.cuda.stream(s):
-        x = _to_device(x_host, dev, "colwise_host")
-        o = _to_device(offs_host, dev, "colwise_host")
         q, sc = colwise(x, o, stream=s, pow2_scales=pow2_scales)
         out_host.copy_(q, non_blocking=True)
         scales_host.copy_(sc, non_blocking=True)
@@ -423,9 +446,9 @@ def rowwise_t_host(a_host, offs_host, out_host=None, scales_host=None, *,
     if scales_host is None:
         scales_host = torch.empty((N, G), dtype=torch.float32, pin_memory=True)
     s = torch.cuda.current_stream(dev) if stream is None else stream
+    a = _to_device(a_host, dev, s, "rowwise_t_host")
+    o = _to_device(offs_host, dev, s, "rowwise_t_host")
     with torch.cuda.stream(s):
-        a = _to_device(a_host, dev, "rowwise_t_host")
-        o = _to_device(offs_host, dev, "rowwise_t_host")
         qt, sc = rowwise_t(a, o, stream=s, pow2_scales=pow2_scales)
         out_host.copy_(qt, non_blocking=True)
         scales_host.copy_(sc, non_blocking=True)

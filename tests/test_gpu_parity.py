@@ -471,3 +471,28 @@ def test_graph_capture_and_replay(gq):
         gq.check_device_error()
         assert_same(q.cpu().numpy(), qs.cpu().numpy(), rq, rs, "colwise in a graph")
         assert_same(qt.cpu().numpy(), ts.cpu().numpy(), tq, trs, "rowwise_t in a graph")
+
+
+def test_host_calls_back_to_back(gq):
+    """Host-buffer calls queued back to back on one stream: each call's
+    host->device copy runs on a side stream and may overlap the previous
+    call's kernel and copies; every result still matches the oracle."""
+    c = synth.random_case("colwise", 1024, 512, 5, seed=91, n_empty=1, align=1, scale_mix=True)
+    r = synth.random_case("rowwise_t", 256, 1040, 6, seed=92, n_empty=1, scale_mix=True)
+    xh = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ah = torch.from_numpy(r.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    xo, ao = torch.from_numpy(c.offs).pin_memory(), torch.from_numpy(r.offs).pin_memory()
+    rq, rs = oracle.colwise(c.x, c.offs)
+    tq, trs = oracle.rowwise_t(r.x, r.offs)
+    s = torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        outs.append(("colwise", gq.colwise_host(xh, xo, stream=s)))
+        outs.append(("rowwise_t", gq.rowwise_t_host(ah, ao, stream=s)))
+    s.synchronize()
+    gq.check_device_error()
+    for kind, (q, sc) in outs:
+        if kind == "colwise":
+            assert_same(q.view(torch.uint8).numpy(), sc.numpy(), rq, rs, "colwise_host")
+        else:
+            assert_same(q.view(torch.uint8).numpy(), sc.numpy(), tq, trs, "rowwise_t_host")
