@@ -10,8 +10,15 @@ travel as their raw ``uint16`` bit patterns, e4m3 results as ``uint8`` codes.
 
 Method source: pytorch/ao pull-request pages #2668 ("use smaller block sizes
 for per group scaling kernels", intro and the kernel arguments in its
-torch.compile failure report) and #2863 ("test and bench new faster method for
-per group rowwise scaling", Summary).
+torch.compile failure report; its MoE fp8 training test for the grouped
+grad_weight product), #2863 ("test and bench new faster method for per group
+rowwise scaling", Summary; its PR stack for the expert weights along dim1)
+and #3114 ("fix mxfp8 a2a bench script; set mxfp8 a2a scaling type to
+RCEIL", Summary: the mxfp8 cast along dim0 and its two scaling types).
+
+Functions: the e4m3 encoder and decoder, the scale (plain and rounded to a
+power of two), colwise, rowwise_t, expert_dim1, mxfp8_dim0 and
+grouped_wgrad.
 """
 from __future__ import annotations
 

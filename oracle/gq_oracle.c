@@ -19,6 +19,9 @@
  *     backward grad_weight GEMM -- groups are contiguous column ranges, one
  *     scale per (row, group) -- and the result is wanted transposed, so the
  *     fp8 output is written as A^T.
+ * Further sections below: stacked expert weights along dim1 (#2863's PR
+ * stack), the mxfp8 cast along dim0 (#3114), and the grouped grad_weight
+ * product of the two quantized operands (#2668's MoE fp8 training test).
  *
  * Per group g with token range [s_g, e_g) and each column (colwise) or row
  * (rowwise):
