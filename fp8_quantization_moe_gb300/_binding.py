@@ -114,12 +114,12 @@ _ws_lock = threading.Lock()
 def _workspace(nbytes: int, device: torch.device, stream_handle: int, kind: int = 0):
     """(buffer, zeroed): a cached device workspace per (device, stream, kind),
     zero-filled when it is allocated.  Calls on one stream run in order, so
-    reuse is safe: the library clears what it uses on every call, except
-    rowwise_t given GQ_WORKSPACE_ZEROED, whose kernel leaves its counters at
-    zero when it ends (its cache is used by rowwise_t alone).  While the
-    stream is being captured into a CUDA graph a missing buffer is not
-    created in the cache (that would synchronise the device): the call gets
-    a fresh one, not known to be zero."""
+    reuse is safe, and every colwise or rowwise_t launch leaves the part of
+    its workspace it used at zero when it ends (also after a bounded wait
+    expired), so calls on a cached buffer pass GQ_WORKSPACE_ZEROED and skip
+    the clear.  While the stream is being captured into a CUDA graph a
+    missing buffer is not created in the cache (that would synchronise the
+    device): the call gets a fresh one, not known to be zero."""
     if nbytes == 0:
         return None, False
     key = (device.index, stream_handle, kind)
@@ -192,12 +192,16 @@ def colwise(x: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
         raise ValueError("colwise: scales must be a contiguous float32 (G, K) tensor")
     sh = _stream_handle(stream, dev)
     need = workspace_bytes(GQ_KIND_COLWISE, M, K, G)
-    ws = workspace if workspace is not None else _workspace(need, dev, sh)[0]
+    flags = GQ_SCALE_POW2 if pow2_scales else 0
+    if workspace is None:
+        ws, zeroed = _workspace(need, dev, sh, GQ_KIND_COLWISE)
+        flags |= GQ_WORKSPACE_ZEROED if zeroed else 0
+    else:
+        ws = workspace
     wp, wn = _ws_ptr(ws)
     with torch.cuda.device(dev):
         st = lib().gq_fp8_colwise_ex(_ptr(x), M, K, _ptr(offs), G, _ptr(out),
-                                     _ptr(scales), GQ_SCALE_POW2 if pow2_scales else 0,
-                                     wp, wn, sh)
+                                     _ptr(scales), flags, wp, wn, sh)
     _check(st, "gq_fp8_colwise")
     return out, scales
 
@@ -227,8 +231,6 @@ def rowwise_t(a: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
     need = workspace_bytes(GQ_KIND_ROWWISE_T, N, Mg, G)
     flags = GQ_SCALE_POW2 if pow2_scales else 0
     if workspace is None:
-        # the cache is zero-filled and only rowwise_t uses it: its counters
-        # are zero whenever a call starts
         ws, zeroed = _workspace(need, dev, sh, GQ_KIND_ROWWISE_T)
         flags |= GQ_WORKSPACE_ZEROED if zeroed else 0
     else:
@@ -261,11 +263,16 @@ def expert_dim1(w: torch.Tensor, *, out=None, scales=None, stream=None, workspac
         raise ValueError("expert_dim1: scales must be a contiguous float32 (E, N) tensor")
     sh = _stream_handle(stream, dev)
     need = workspace_bytes(GQ_KIND_COLWISE, E * K, N, E)
-    ws = workspace if workspace is not None else _workspace(need, dev, sh)[0]
+    flags = GQ_SCALE_POW2 if pow2_scales else 0
+    if workspace is None:  # the colwise kernel: the colwise cache
+        ws, zeroed = _workspace(need, dev, sh, GQ_KIND_COLWISE)
+        flags |= GQ_WORKSPACE_ZEROED if zeroed else 0
+    else:
+        ws = workspace
     wp, wn = _ws_ptr(ws)
     with torch.cuda.device(dev):
         st = lib().gq_fp8_expert_dim1(_ptr(w), E, K, N, _ptr(out), _ptr(scales),
-                                      GQ_SCALE_POW2 if pow2_scales else 0, wp, wn, sh)
+                                      flags, wp, wn, sh)
     _check(st, "gq_fp8_expert_dim1")
     return out, scales
 

@@ -143,25 +143,11 @@ gq_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype,
   return GQ_OK;
 }
 
-int32_t schedule_lag(int32_t forced, int64_t units, int64_t groups, int64_t grid) {
-  // Phase A of slab d + lag is claimed right before phase B of slab d, so
-  // phase B starts about lag * units tickets after slab d's last phase-A
-  // ticket.  A lead of about 1.7 tickets per block -- the tickets each block
-  // holds in flight, plus the blocks' drift -- keeps phase B from waiting for
-  // its slab; a longer one only widens what L2 must hold between a tile's two
-  // reads (measured on the 32768- and 65536-row workloads: the best lead
-  // was 512 tickets on 304 blocks at both sizes).
-  int64_t lag = forced > 0 ? forced : (17 * grid + 5 * units) / (10 * units);
-  if (lag < 1) lag = 1;
-  if (lag > groups) lag = groups;
-  return static_cast<int32_t>(lag);
-}
-
 WorkspaceLayout colwise_workspace(int64_t K, int64_t G) {
   auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
   WorkspaceLayout L;
   L.counters = 256;
-  L.amax = L.counters + up(static_cast<size_t>((K + 63) / 64) * 4);
+  L.amax = L.counters + up(static_cast<size_t>(G * ((K + colwise::kW - 1) / colwise::kW)) * 4);
   L.total = L.amax + up(static_cast<size_t>(G * K) * 4);
   return L;
 }
@@ -189,8 +175,8 @@ using namespace gq;
 
 namespace {
 
-constexpr uint32_t kKnownFlags = GQ_SCALE_POW2;  // every call
-constexpr uint32_t kRowwiseFlags = GQ_SCALE_POW2 | GQ_WORKSPACE_ZEROED;
+// every call that takes a workspace knows both flags
+constexpr uint32_t kKnownFlags = GQ_SCALE_POW2 | GQ_WORKSPACE_ZEROED;
 
 gq_status validate_common(const void* in, const void* out, const int32_t* offs,
                           int32_t n_groups, const float* scales, int64_t rows,
@@ -342,8 +328,8 @@ gq_status gq_fp8_rowwise_t_ex(const void* a, int64_t N, int64_t Mg,
                               float* scales, uint32_t flags, void* workspace,
                               size_t workspace_bytes, gq_stream_t stream) {
   const char* name = "gq_fp8_rowwise_t";
-  if (flags & ~kRowwiseFlags)
-    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kRowwiseFlags);
+  if (flags & ~kKnownFlags)
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kKnownFlags);
   gq_status st = validate_common(a, out_t, offs, n_groups, scales, N, Mg, name);
   if (st != GQ_OK) return st;
   if (N % 16 != 0)

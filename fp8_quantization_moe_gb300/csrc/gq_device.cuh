@@ -1,57 +1,17 @@
-// gq_device.cuh -- device building blocks shared by the two quantization
-// kernels: inline-PTX wrappers (mbarrier, TMA, cp.async, L2 policies, e4m3
-// convert), bounded waits, the group-end table, tile headers and the ticket
-// schedule.
+// gq_device.cuh -- device building blocks shared by the kernels of
+// libgqfp8: inline-PTX wrappers (mbarrier, TMA loads and stores, cp.async,
+// L2 cache policies, shared-memory loads, ldmatrix, bf16 |x| maxima, the
+// e4m3 convert), bounded waits, the scale of an amax, and the group-end
+// table.  Each kernel describes its own execution model in its file:
+//   gq_colwise.cu  (group, slab) strips: resident strips in one pass, longer
+//                  ones in two phases through L2, tickets from a counter;
+//   gq_rowwise.cu  block-local (row band, group) units, one HBM read;
+//   gq_mxfp8.cu    a plain coalesced stream;
+//   gq_wgrad.cu    a tcgen05 grouped GEMM.
 //
-// Execution model (both kernels).  A persistent grid, launched cooperatively
-// so that every CTA is resident, of CTAs with four roles: a context warp, a
-// producer warp, consumer warps and a signal lane.
-//
-// Work comes in tickets: super tiles of kSub stages (256 consecutive tokens
-// of one column slab or row band; a stage is 8 KB).  Each super tile is
-// visited twice: in phase A the |x| maxima of its stages are folded into
-// per-(group, column) or per-(row, group) amax words with atomicMax; in
-// phase B, once every phase-A super tile its amax words depend on is done,
-// it is re-read, scaled and cast.  Tiles that share amax words form a
-// "dependency group" (a column slab for colwise, a row band for rowwise_t).
-// Tickets are numbered in an order in which phase A of dependency group d+L
-// precedes phase B of group d (L = the lag), so that by the time phase B of
-// a group comes up its phase-A tiles are finished and its bytes still sit in
-// L2 (loaded with evict_last): HBM sees one read of the input.  CTAs claim
-// tickets from a global counter, so tickets are taken roughly in that order
-// whatever the pace of each CTA.
-//
-// The context warp claims the CTA's tickets, one ahead, and writes a context
-// per ticket into a small ring: first the ticket itself (published at once,
-// so that the producer can start loading), then -- in phase B after the
-// dependency group is complete -- the super tile's header (its group
-// segments) and the amax words of its first segments, copied with cp.async.
-// The producer warp follows the published tickets and loads their stages,
-// in order, into a shared ring of stage buffers with TMA, tagging each with
-// its ticket and place.  A consumer warp takes the next loaded stage (a
-// shared counter), whichever ticket it belongs to, and does all the work of
-// that stage alone, with no barrier among warps, so the per-stage
-// bookkeeping (the waits, the segment walk, the scale divisions) is paid
-// once per 8 KB.  In phase A the warps fold their stage maxima into the
-// context with shared-memory atomics; the warp that finishes a super tile's
-// last stage (an acquire-release counter in the context tells it) adds them
-// to the global amax words, one atomicMax per (segment, column or row), and
-// posts the super tile to the signal lane.
-//
-// The signal lane runs an event loop with two jobs.  (1) Finished phase-A
-// super tiles reach it through a small ring of shared-memory slots; it
-// publishes them on the groups' done counters with release reductions, so
-// the memory fence that publishing implies never stalls a consumer.  (2)
-// When the context warp waits for a dependency group, it polls the group's
-// done counter (acquire) and then raises a shared-memory flag (release).
-//
-// Progress: all CTAs are resident and each processes its tickets in
-// increasing order, so the smallest unfinished ticket can always advance --
-// its phase-A dependencies have smaller tickets, claimed by running CTAs;
-// within a CTA, stages are loaded and claimed in ticket order, so the stages
-// of a ticket never wait behind those of a later one -- and the schedule
-// cannot deadlock; the signal lane never blocks on a dependency while
-// completions wait in its ring.  Every wait is nonetheless bounded in time.
+// Every wait on another warp or block is bounded by %globaltimer: on expiry
+// the waiter records a bit in the per-device error word and returns false,
+// so a kernel ends instead of hanging and the host reports GQ_ERR_TIMEOUT.
 #pragma once
 
 #include <cuda.h>
@@ -68,23 +28,6 @@ constexpr int kMaxGroups = 1024;   // GQ_MAX_GROUPS
 // error-word bits
 constexpr unsigned kErrDepTimeout = 1u;   // a dependency-group wait expired
 constexpr unsigned kErrMbarTimeout = 2u;  // an mbarrier wait expired
-
-// ------------------------------------------------------------ tile header --
-// Header of a super tile, written by the context warp into a context and
-// read by the consumers once the context is full.  Segment
-// bounds are relative to lo.
-template <int kMaxSeg>
-struct alignas(16) TileHdr {
-  int32_t phase;   // 0 = A (amax), 1 = B (scale + cast)
-  int32_t dg;      // dependency group
-  int32_t lo, hi;  // token range [lo, hi) of the super tile, clamped to the extent
-  int32_t own_lo, own_hi;  // groups whose scales phase B of this tile writes
-  int32_t nseg;            // nonempty group segments inside [lo, hi)
-  int32_t nsub;            // stages of the super tile (a short last tile has fewer)
-  int16_t seg_g[kMaxSeg];
-  uint16_t seg_lo[kMaxSeg];
-  uint16_t seg_hi[kMaxSeg];
-};
 
 // ---------------------------------------------------------- PTX wrappers --
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -416,113 +359,6 @@ __device__ __forceinline__ void build_ends(const int32_t* __restrict__ offs, int
   }
 }
 
-// The header of the tile with token range [lo, hi), built by one warp from
-// the group-end table: the nonempty group segments in the tile and the range
-// of groups whose scales the tile owns (the groups starting inside it; the
-// last tile of the token extent also owns those starting at or after its
-// start).  Groups are examined 32 at a time, from the block that holds the
-// first group ending at or after lo (found by probing the block ends).
-template <int kMaxSeg>
-__device__ __forceinline__ void build_header_warp(TileHdr<kMaxSeg>& h,
-                                                  const int32_t* ends, int n,
-                                                  int32_t lo, int32_t hi,
-                                                  bool last, int lane) {
-  int b0 = 0;
-  if (n > 32) {  // n <= 1024: one probe per block end
-    const int pe = 32 * lane + 31;
-    const unsigned m = __ballot_sync(0xffffffffu, pe >= n || ends[pe] >= lo);
-    b0 = m ? __ffs(m) - 1 : 32;  // 32: no group ends at or after lo
-  }
-  const unsigned lt = (1u << lane) - 1u;
-  int ns = 0, own_lo = n, own_hi = 0;
-  for (int b = b0; 32 * b < n; ++b) {
-    const int g = 32 * b + lane;
-    const bool valid = g < n;
-    const int32_t s = valid ? (g ? ends[g - 1] : 0) : 0;
-    const int32_t e = valid ? ends[g] : 0;
-    const bool seg = valid && s < hi && e > lo && s < e;
-    const bool own = valid && s >= lo && (last || s < hi);
-    const unsigned ms = __ballot_sync(0xffffffffu, seg);
-    const unsigned mo = __ballot_sync(0xffffffffu, own);
-    if (seg) {
-      const int pos = ns + __popc(ms & lt);
-      if (pos < kMaxSeg) {
-        h.seg_g[pos] = static_cast<int16_t>(g);
-        h.seg_lo[pos] = static_cast<uint16_t>(max(s, lo) - lo);
-        h.seg_hi[pos] = static_cast<uint16_t>(min(e, hi) - lo);
-      }
-    }
-    ns += __popc(ms);
-    if (mo) {  // owned groups are contiguous
-      own_lo = min(own_lo, 32 * b + __ffs(mo) - 1);
-      own_hi = 32 * b + 32 - __clz(mo);
-    }
-    // starts are nondecreasing: once a start reaches hi, no later group has
-    // a segment here, and only the last tile owns groups starting later
-    if (!last && __ballot_sync(0xffffffffu, valid && s < hi) != 0xffffffffu) break;
-  }
-  if (lane == 0) {
-    h.lo = lo;
-    h.hi = hi;
-    h.nseg = min(ns, kMaxSeg);
-    h.own_lo = own_hi > 0 ? own_lo : 0;
-    h.own_hi = own_hi;
-  }
-}
-
-// ---------------------------------------------------------- ticket order --
-struct Schedule {
-  int32_t units;   // tiles per dependency group (>= 1)
-  int32_t groups;  // dependency groups (>= 1)
-  int32_t lag;     // 1 <= lag <= groups
-};
-
-// Tickets come in blocks of `units` (one dependency group, one phase), in
-// the order
-//   A(0) .. A(L-1), then A(L), B(0), A(L+1), B(1), ..., A(G-1), B(G-1-L),
-//   then B(G-L) .. B(G-1).
-// Block b holds tickets b * units .. b * units + units - 1; the unit is the
-// ticket's place in its block.  Returns the phase (0 = A, 1 = B) and group.
-__device__ __forceinline__ void decode_block(int32_t b, const Schedule& s,
-                                             int32_t& phase, int32_t& dg) {
-  if (b < s.lag) {
-    phase = 0;
-    dg = b;
-    return;
-  }
-  const int32_t i = b - s.lag;
-  const int32_t pairs = s.groups - s.lag;
-  if (i < 2 * pairs) {
-    phase = i & 1;
-    dg = (i & 1) ? (i >> 1) : s.lag + (i >> 1);
-  } else {
-    phase = 1;
-    dg = pairs + (i - 2 * pairs);
-  }
-}
-
-// Walks tickets first, first + stride, first + 2 stride, ... as (block,
-// unit) pairs without a division per step.
-struct TicketWalk {
-  int32_t block, unit;
-  int32_t q, r;  // stride = q * units + r
-  __device__ __forceinline__ TicketWalk(uint32_t first, uint32_t stride,
-                                        int32_t units) {
-    block = static_cast<int32_t>(first / static_cast<uint32_t>(units));
-    unit = static_cast<int32_t>(first % static_cast<uint32_t>(units));
-    q = static_cast<int32_t>(stride / static_cast<uint32_t>(units));
-    r = static_cast<int32_t>(stride % static_cast<uint32_t>(units));
-  }
-  __device__ __forceinline__ void next(int32_t units) {
-    block += q;
-    unit += r;
-    if (unit >= units) {
-      unit -= units;
-      ++block;
-    }
-  }
-};
-
 // Four e4m3 bytes from two bf16x2 words w0 = (x0, x1), w1 = (x2, x3) and
 // four scales: byte i = e4m3(fp32(x_i * s_i)), x0 in the lowest byte.  The
 // products are IEEE fp32 multiplies rounded to nearest even (mul.rn.f32x2,
@@ -563,160 +399,7 @@ __device__ __forceinline__ uint2 quant8(uint4 v, const float* sc) {
                     quant4(v.z, v.w, sc[4], sc[5], sc[6], sc[7]));
 }
 
-// ----------------------------------------------------------- signal ring --
-// Consumer warps -> signal lane: one slot per finished phase-A super tile, taken
-// in the order of a shared claim counter.  A slot's full barrier counts the
-// posting warp's lane-0 arrival (after __syncwarp, which orders the warp's
-// amax atomics before it); its empty barrier the signal lane's.  Only the
-// warp that flushes a super tile's maxima posts it.
-template <int kSlots>
-struct SigRing {
-  uint64_t full[kSlots];
-  uint64_t empty[kSlots];
-  int32_t dg[kSlots];
-  uint32_t head;  // next slot sequence number to claim
-};
-
-constexpr int32_t kSigEnd = -1;   // a consumer warp is done
-constexpr int32_t kSigSkip = -2;  // a completion withheld (test hook)
-
-template <int kSlots>
-__device__ __forceinline__ void sig_init(SigRing<kSlots>& r) {
-  for (int i = 0; i < kSlots; ++i) {
-    mbar_init(&r.full[i], 1);
-    mbar_init(&r.empty[i], 1);
-  }
-  r.head = 0;
-}
-
-// Called by a whole consumer warp: hands over a finished phase-A super tile of
-// dependency group dg >= 0, kSigSkip or kSigEnd.  At most one post per warp
-// is outstanding and there are fewer warps than slots, so a claimed slot's
-// previous round is the one its empty barrier last completed.
-template <int kSlots>
-__device__ __forceinline__ void sig_post(SigRing<kSlots>& r, int32_t dg, int lane,
-                                         uint64_t timeout_ns, unsigned* err) {
-  __syncwarp();
-  if (lane == 0) {
-    const uint32_t seq = atomicAdd(&r.head, 1u);
-    const int slot = static_cast<int>(seq % kSlots);
-    mbar_wait(&r.empty[slot], ((seq / kSlots) & 1u) ^ 1u, timeout_ns, err);
-    r.dg[slot] = dg;
-    mbar_arrive(&r.full[slot]);
-  }
-  __syncwarp();
-}
-
-// Dependency readiness, shared by the context warp and the signal lane.
-struct DepFlag {
-  int32_t want;   // dependency group the context warp waits for (-1: none)
-  int32_t ready;  // largest dependency group seen complete (-1: none)
-  int32_t fail;   // 1 once the signal lane gave up waiting
-};
-
-__device__ __forceinline__ void dep_init(DepFlag& f) {
-  f.want = -1;
-  f.ready = -1;
-  f.fail = 0;
-}
-
-// The signal lane's event loop.  (1) Takes the posted slots in order -- all
-// that are posted each time round -- and adds each run of equal groups to
-// that group's done counter with one release reduction.  (2) When the
-// context warp waits for a dependency group (f.want), probes the group's done
-// counter (acquire) once per round and, when it has reached `target`,
-// publishes the group in f.ready (release).  It never blocks on a
-// dependency, so this CTA's own completions keep flowing.  Returns after
-// `posters` kSigEnd posts.  Gives up a dependency after timeout_ns
-// (kErrDepTimeout, f.fail = 1) and the ring after idle_ns without any event.
-template <int kSlots>
-__device__ __forceinline__ void signal_lane(SigRing<kSlots>& r, DepFlag& f,
-                                            uint32_t* done, uint32_t target, int posters,
-                                            uint64_t timeout_ns, uint64_t idle_ns,
-                                            unsigned* err) {
-  uint32_t seq = 0;
-  int ended = 0;
-  int32_t ready = -1, watched = -1;
-  uint64_t t_event = global_timer_ns(), t_want = t_event;
-  for (;;) {
-    bool progress = false, stop = false;
-    int32_t run_dg = -1;
-    uint32_t run = 0;
-    for (int n = 0; n < kSlots; ++n) {
-      const int slot = static_cast<int>(seq % kSlots);
-      if (!mbar_test_wait(&r.full[slot], (seq / kSlots) & 1u)) break;
-      const int32_t dg = r.dg[slot];
-      mbar_arrive(&r.empty[slot]);
-      ++seq;
-      progress = true;
-      if (dg == kSigEnd) {
-        if (++ended == posters) {
-          stop = true;
-          break;
-        }
-        continue;
-      }
-      if (dg >= 0) {
-        if (dg != run_dg) {
-          if (run) red_release_add(done + run_dg, run);
-          run_dg = dg;
-          run = 0;
-        }
-        ++run;
-      }
-    }
-    if (run) red_release_add(done + run_dg, run);
-    if (stop) return;
-    const uint64_t now = global_timer_ns();
-    const int32_t want = *reinterpret_cast<volatile int32_t*>(&f.want);
-    if (want != watched) {
-      watched = want;
-      t_want = now;
-    }
-    if (want > ready) {
-      if (ld_acquire_u32(done + want) >= target) {
-        ready = want;
-        st_release_cta_s32(&f.ready, want);
-        progress = true;
-      } else if (ld_volatile_u32(err) != 0u || now - t_want > timeout_ns) {
-        if (ld_volatile_u32(err) == 0u) atomicOr(err, kErrDepTimeout);
-        st_release_cta_s32(&f.fail, 1);
-      }
-    }
-    if (progress) {
-      t_event = now;
-    } else {
-      if (now - t_event > idle_ns) {
-        atomicOr(err, kErrMbarTimeout);
-        st_release_cta_s32(&f.fail, 1);
-        return;
-      }
-      __nanosleep(want > ready ? 64 : 256);
-    }
-  }
-}
-
-// Context-warp side: announces dependency group dg and waits until it is
-// complete.  False when the signal lane gave up, an error is recorded
-// elsewhere, or timeout_ns passes.
-__device__ __forceinline__ bool wait_dep_flag(DepFlag& f, int32_t dg,
-                                              uint64_t timeout_ns, unsigned* err) {
-  if (ld_acquire_cta_s32(&f.ready) >= dg) return true;
-  *reinterpret_cast<volatile int32_t*>(&f.want) = dg;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (ld_acquire_cta_s32(&f.ready) >= dg) return true;
-    if (ld_acquire_cta_s32(&f.fail) != 0) return false;
-    if (global_timer_ns() - t0 > timeout_ns) {
-      atomicOr(err, kErrDepTimeout);
-      return false;
-    }
-    __nanosleep(32);
-  }
-}
-
-// Tickets are claimed from a global counter, in increasing order; ticket t
-// is unit t % units of block t / units.
+// Tickets are claimed from a global counter, in increasing order.
 __device__ __forceinline__ uint32_t claim_ticket(uint32_t* counter) {
   return atomicAdd(counter, 1u);
 }

@@ -28,11 +28,6 @@ struct DebugKnobs {
   int32_t lag[2] = {0, 0};  // per kind; 0 = automatic
 };
 
-// The lag of the colwise ticket order: `forced` if positive, else the
-// number of slabs (of `units` tickets each) closest to a lead of 1.7
-// tickets per block of the `grid`; clamped to [1, groups].
-int32_t schedule_lag(int32_t forced, int64_t units, int64_t groups, int64_t grid);
-
 // Encodes a 2-D tiled tensor map (row-major, dim0 innermost).
 gq_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype,
                           void* base, uint64_t dim0, uint64_t dim1,
@@ -45,19 +40,19 @@ gq_status fail(gq_status st, const char* fmt, ...);
 // Returns GQ_ERR_CUDA with the runtime's message if `e` is an error.
 gq_status check_cuda(cudaError_t e, const char* what);
 
-// Colwise workspace layout: a 256-byte header (the ticket counter first),
-// then one counter per 64 columns (the kernel uses one per 128-column slab),
-// then the (G, K) amax words.  Offsets in bytes; every region starts on a
-// 256-byte boundary.
+// Colwise workspace layout: a 256-byte header (work counters), one counter
+// per (group, 128-column slab) strip, then the (G, K) amax words.  Offsets
+// in bytes; every region starts on a 256-byte boundary.  Every launch
+// leaves all of it zero.
 struct WorkspaceLayout {
-  size_t counters = 0;  // start of the counters
+  size_t counters = 0;  // start of the strip counters
   size_t amax = 0;      // start of the amax words
   size_t total = 0;
 };
 WorkspaceLayout colwise_workspace(int64_t K, int64_t G);
 
 namespace colwise {
-constexpr int kW = 128;  // columns per slab (dependency group)
+constexpr int kW = 128;  // columns per slab
 gq_status setup(DeviceInfo& info);
 // offs == nullptr: G groups of `uniform` rows each.
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,

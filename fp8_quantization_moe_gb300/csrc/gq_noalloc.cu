@@ -13,7 +13,9 @@
 // Nothing here allocates.  The first call on each device looks up the
 // array's device address with cudaGetSymbolAddress, with that device
 // current; a host-side name of a __device__ array is not a device address,
-// so the kernel must never be handed `g_noalloc_scratch` itself.  The actual
+// so the kernel must never be handed `g_noalloc_scratch` itself.  Only a
+// successful lookup is kept: a lookup that failed (for instance one made
+// while the stream was being captured) is tried again on the next call.  The actual
 // work goes through the same validation and kernel as gq_fp8_colwise, which
 // clears the used part of the scratch with cudaMemsetAsync on the caller's
 // stream before the kernel runs.
@@ -29,15 +31,25 @@ static_assert(kScratchBytes % 256 == 0, "scratch size keeps 256-byte alignment")
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+void* g_scratch_addr[kMaxDevices];  // null until a lookup succeeded
+std::mutex g_scratch_mu;
 
-// Once per device, with that device current.
-void lookup_scratch(int dev) {
-  void* p = nullptr;
-  g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-  g_scratch_addr[dev] = p;
+// The array's device address on `dev` (the current device), looked up on
+// the first call that succeeds and kept from then on.
+cudaError_t scratch_address(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      cudaGetLastError();  // leave no stale error for a later launch check
+      return e;
+    }
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -66,11 +78,13 @@ extern "C" gq_status gq_fp8_colwise_noalloc(const void* x, int64_t M, int64_t K,
   if (dev < 0 || dev >= kMaxDevices)
     return gq::fail(GQ_ERR_UNSUPPORTED,
                     "gq_fp8_colwise_noalloc: device ordinal %d out of range", dev);
-  std::call_once(g_scratch_once[dev], lookup_scratch, dev);
-  if (g_scratch_err[dev] != cudaSuccess || g_scratch_addr[dev] == nullptr)
+  void* scratch = nullptr;
+  const cudaError_t le = scratch_address(dev, &scratch);
+  if (le != cudaSuccess)
     return gq::fail(GQ_ERR_CUDA,
-                    "gq_fp8_colwise_noalloc: scratch address lookup failed: %s",
-                    cudaGetErrorString(g_scratch_err[dev]));
-  return gq_fp8_colwise(x, M, K, offs, n_groups, out, scales,
-                        g_scratch_addr[dev], kScratchBytes, stream);
+                    "gq_fp8_colwise_noalloc: scratch address lookup failed "
+                    "(tried again on the next call): %s",
+                    cudaGetErrorString(le));
+  return gq_fp8_colwise(x, M, K, offs, n_groups, out, scales, scratch,
+                        kScratchBytes, stream);
 }

@@ -37,7 +37,10 @@
  * the quantization calls, which are asynchronous on `stream` (a
  * cudaStream_t; NULL is the legacy default stream).  Outputs and the
  * workspace must stay valid until the stream's work completes.  Concurrent
- * calls must use distinct workspaces.
+ * calls must use distinct workspaces.  The library keeps per-device state
+ * (launch set-up, the device addresses of its own __device__ arrays) for the
+ * life of the process, so no gq_* call may follow a cudaDeviceReset of that
+ * device in the same process.
  *
  * Errors.  Every condition the host can check returns a status before any
  * work is enqueued; nothing aborts.  Failures of the CUDA runtime during
@@ -78,13 +81,14 @@ typedef enum gq_status {
  * Workspace size in bytes for one call.
  *   kind GQ_KIND_COLWISE:   rows = M, cols = K.
  *   kind GQ_KIND_ROWWISE_T: rows = N, cols = Mg.
- * Colwise: a work counter, one completion counter per column slab (128
- * columns) and the per-(group, column) running amax words.  Rowwise_t: a
- * work counter and a finished-blocks counter (256 bytes), since each (row
- * band, group) pair is finished by one thread block.  The call clears what
- * it uses itself, so the contents on entry do not matter (rowwise_t with
- * GQ_WORKSPACE_ZEROED skips the clear; see there).  Returns 0 when no
- * workspace is needed (empty problems) and for invalid arguments.
+ * Colwise: a work counter, a finished-blocks counter, one counter per
+ * (group, 128-column slab) strip and the per-(group, column) running amax
+ * words.  Rowwise_t: a work counter and a finished-blocks counter (256
+ * bytes), since each (row band, group) pair is finished by one thread
+ * block.  The call clears what it uses itself, so the contents on entry do
+ * not matter (with GQ_WORKSPACE_ZEROED the call skips the clear; see
+ * there).  Returns 0 when no workspace is needed (empty problems) and for
+ * invalid arguments.
  */
 size_t gq_workspace_bytes(int kind, int64_t rows, int64_t cols,
                           int32_t n_groups);
@@ -148,13 +152,14 @@ gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,
  */
 #define GQ_SCALE_POW2 1u
 /*
- *   GQ_WORKSPACE_ZEROED  (gq_fp8_rowwise_t_ex only; GQ_ERR_INVALID_ARG
- *                  elsewhere) the caller states that the first 8 bytes of
- *                  the workspace are zero -- zero-filled once, or left so by
- *                  an earlier rowwise_t call that completed: every rowwise_t
- *                  launch returns its counters to zero before it ends, also
- *                  after a bounded wait expired -- and the call skips its own
- *                  clear of them (one device operation less per call).
+ *   GQ_WORKSPACE_ZEROED  the caller states that the workspace holds
+ *                  zeros where this call uses it -- zero-filled once, or
+ *                  left so by an earlier call of the same library on it
+ *                  that completed: every colwise, expert_dim1 and rowwise_t
+ *                  launch returns the part of its workspace it used to zero
+ *                  before it ends, also after a bounded wait expired -- and
+ *                  the call skips its own clear (one device operation less
+ *                  per call).
  */
 #define GQ_WORKSPACE_ZEROED 2u
 
@@ -183,7 +188,7 @@ gq_status gq_fp8_rowwise_t_ex(const void* a, int64_t N, int64_t Mg,
  *            E * K < 2^31.
  *   out      e4m3 bytes [E, K, N] row-major, 16-byte aligned.    (output)
  *   scales   fp32 [E, N] row-major: scale of expert e, column n. (output)
- *   flags    0 or GQ_SCALE_POW2.
+ *   flags    0, GQ_SCALE_POW2, GQ_WORKSPACE_ZEROED or both.
  *   workspace, workspace_bytes: at least gq_workspace_bytes(GQ_KIND_COLWISE,
  *            E * K, N, E) bytes, 256-byte aligned.
  *   stream   the CUDA stream to run on.
@@ -265,7 +270,8 @@ gq_status gq_grouped_wgrad(const void* qa_t, const float* sa, const void* qx, co
  *     larger calls return GQ_ERR_UNSUPPORTED before enqueueing anything.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  Only a successful lookup is kept: if it
+ *     fails (GQ_ERR_CUDA), the next call on that device tries again.
  *   - Each call clears the part of the array it uses (cudaMemsetAsync on
  *     `stream`), so leftovers of an earlier call do not matter.
  *   - All calls on a device share the array: calls whose GPU work may
@@ -297,9 +303,9 @@ int gq_version(void);
 /*
  * Test hook for the bounded waits.  wait_timeout_ns sets the limit after
  * which a waiting kernel gives up (0 restores the 1 s default).
- * skip_arrival != 0 makes the next launches omit one completion signal --
- * colwise: the first phase-A tile of the first column slab, whose waiters
- * are other thread blocks; rowwise_t: the amax-complete signal of the
+ * skip_arrival != 0 makes the next launches omit completion signals --
+ * colwise: the first phase-A tile of every two-phase strip of the first
+ * column slab, whose waiters are other thread blocks; rowwise_t: the amax-complete signal of the
  * (first row band, first group) unit, whose waiters are the warps that
  * would cast it; grouped_wgrad: the release of thread block 0's first TMEM
  * accumulator, whose waiter is the block's MMA warp -- so that the waiters
@@ -310,12 +316,13 @@ gq_status gq_debug_set(int skip_arrival, int64_t wait_timeout_ns);
 
 /*
  * Tuning knob for the phase interleave of `kind`.  The colwise kernel
- * visits every tile twice -- phase A (amax) and phase B (scale + cast) --
- * and gives phase A a lead of `lag` column slabs (128 columns each): phase
- * A of slab d + lag is scheduled before phase B of slab d.  A longer lead
- * keeps phase B from waiting on unfinished amax words; a shorter one keeps
- * the re-read tiles in L2.  lag = 0 restores the automatic choice; larger
- * values are clamped to the number of slabs.  Results do not depend on it.
+ * visits every tile of a group strip longer than 256 rows twice -- phase A
+ * (amax) and phase B (scale + cast) -- and gives phase A a lead of `lag`
+ * column slabs (128 columns each): phase A of slab d + lag is scheduled
+ * alongside phase B of slab d.  A longer lead keeps phase B from waiting on
+ * unfinished amax words; a shorter one keeps the re-read tiles in L2.
+ * lag = 0 restores the automatic choice; larger values are clamped to the
+ * number of slabs.  Results do not depend on it.
  * GQ_KIND_ROWWISE_T is accepted and has no effect: that kernel has no
  * cross-block schedule.  Process-wide; not thread-safe with concurrent
  * calls.  Returns GQ_ERR_INVALID_ARG for an unknown kind or a negative lag.

@@ -56,9 +56,12 @@ def test_status_strings(gq):
 
 
 def test_workspace_bytes(gq):
-    # colwise 65536x4096, 16 groups: 256 B header + 32 slab counters (256 B)
-    # + 16*4096 amax words
-    assert gq.workspace_bytes(0, 65536, 4096, 16) == 256 + 256 + 16 * 4096 * 4
+    # colwise 65536x4096, 16 groups: 256 B header + 16 x 32 strip counters
+    # (2 KiB) + 16*4096 amax words
+    assert gq.workspace_bytes(0, 65536, 4096, 16) == 256 + 2048 + 16 * 4096 * 4
+    # regions padded to 256 bytes: 3 groups x 2 slabs (K = 144), 3 x 144
+    # amax words
+    assert gq.workspace_bytes(0, 100, 144, 3) == 256 + 256 + 1792
     # rowwise_t: a unit counter and a finished-blocks counter, padded
     assert gq.workspace_bytes(1, 8192, 16640, 64) == 256
     assert gq.workspace_bytes(0, 0, 4096, 4) == 0
@@ -139,7 +142,7 @@ def test_ex_calls_reject_unknown_flags(gq):
     lib = gq.lib()
     assert gq.GQ_SCALE_POW2 == 1
     assert gq.GQ_WORKSPACE_ZEROED == 2
-    for bad in (2, 0x80000000, 3):   # GQ_WORKSPACE_ZEROED is rowwise_t's alone
+    for bad in (4, 0x80000000, 7):
         assert lib.gq_fp8_colwise_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1
     for bad in (4, 0x80000000, 7):
         assert lib.gq_fp8_rowwise_t_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1

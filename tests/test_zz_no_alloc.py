@@ -6,7 +6,8 @@ path that must not call cudaMalloc because it can synchronise the device).
 Its scratch is a fixed array inside the library, so the test checks that two
 calls in a row -- the second with much smaller magnitudes, which would expose
 amax words left over from the first -- give the same bytes as gq_fp8_colwise
-with a caller workspace, and that a call too large for the array is refused.
+with a caller workspace and as the CPU oracle, and that a call too large for
+the array is refused.
 
 The file name makes pytest collect it last.
 """
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from fp8_quantization_moe_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -80,6 +82,11 @@ def test_noalloc_matches_workspace_path_twice(gq):
         assert lib.gq_check_device_error(stream) == 0
         assert torch.equal(q1, q2), case.name
         assert torch.equal(s1.view(torch.int32), s2.view(torch.int32)), case.name
+        # and the oracle, byte for byte (rows past the last group keep 0x5A)
+        rq, rs = oracle.colwise(case.x, case.offs,
+                                out=np.full((M, K), 0x5A, np.uint8))
+        assert np.array_equal(q1.cpu().numpy(), rq), case.name
+        assert np.array_equal(s1.cpu().numpy().view(np.uint32), rs.view(np.uint32)), case.name
         del ws
 
 
