@@ -504,6 +504,146 @@ def run_wgrad(args):
     return 0
 
 
+def _time_calls(fn, steps, flush=None):
+    """Median and mean microseconds of `steps` calls of fn, each bracketed by
+    CUDA events on the current stream; `flush` (untimed) runs before each.
+    Everything is enqueued back to back and synchronised once, so that the
+    host's launch latency stays outside the events."""
+    import torch
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    per = [e0.elapsed_time(e1) * 1e3 for e0, e1 in ev]
+    return statistics.median(per), statistics.mean(per)
+
+
+def per_config_block(dev, steps: int = 20):
+    """Every listed workload and group count, and the built NEXT rows, each
+    timed on its own: us per call (median of `steps`, CUDA events around each
+    C-ABI call), algorithmic GB/s (2 B read + 1 B written per element + 4 B
+    per fp32 scale, 1 B per e8m0 scale) and % of the measured copy peak; the
+    grouped grad_weight GEMM as TFLOP/s against the measured bf16 figures
+    times the nominal fp8/bf16 ratio.  Inputs that fit L2 (workloads 1 and
+    2) get an L2 flush (a 256 MiB write) before each timed call."""
+    import numpy as np
+    import torch
+
+    import fp8_quantization_moe_gb300 as gq
+    from fp8_quantization_moe_gb300 import synth
+
+    peak, _ = measured_peaks()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    def rec(us_med, us_mean, nbytes, **extra):
+        gbs = nbytes / (us_med * 1e-6) / 1e9
+        d = {"us": round(us_med, 2), "us_mean": round(us_mean, 2), "gbs": round(gbs, 1),
+             "pct_peak": round(100 * gbs / peak, 1)}
+        d.update(extra)
+        return d
+
+    def bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    out = {}
+    # colwise: workloads 1, 2 (and 2 with every strip two-phase), 3 at 4 / 8 / 16 groups
+    for idx, groups in ((1, 4), (2, 16), (3, 4), (3, 8), (3, 16)):
+        case = synth.workload(idx, groups)
+        M, K = case.x.shape
+        x, o = bf16(case.x), torch.from_numpy(case.offs).to(dev)
+        q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+        sc = torch.empty((groups, K), dtype=torch.float32, device=dev)
+        small = 2 * M * K < (64 << 20)
+        for two in ((False, True) if idx == 2 else (False,)):
+            med, mean = _time_calls(lambda: gq.colwise(x, o, out=q, scales=sc, two_phase=two),
+                                    steps, flush if small else None)
+            name = f"colwise_{M}x{K}_g{groups}" + ("_two_phase" if two else "")
+            out[name] = rec(med, mean, colwise_bytes(M, K, groups),
+                            l2="flushed before each call" if small else "input larger than L2")
+        del x, q
+    torch.cuda.empty_cache()
+    # rowwise_t: workload 4 (16 groups), 5 at 1 and 64 groups
+    for idx, groups in ((4, 16), (5, 1), (5, 64)):
+        case = synth.workload(idx, groups)
+        N, Mg = case.x.shape
+        a, o = bf16(case.x), torch.from_numpy(case.offs).to(dev)
+        qt = torch.empty((Mg, N), dtype=torch.float8_e4m3fn, device=dev)
+        sc = torch.empty((N, groups), dtype=torch.float32, device=dev)
+        med, mean = _time_calls(lambda: gq.rowwise_t(a, o, out=qt, scales=sc), steps)
+        out[f"rowwise_t_{N}x{Mg}_g{groups}"] = rec(med, mean, rowwise_bytes(N, Mg, groups),
+                                                   l2="input larger than L2")
+        del a, qt
+    torch.cuda.empty_cache()
+    # mxfp8 dim0 on workload 3's X
+    case = synth.workload(3, 16)
+    M, K = case.x.shape
+    x = bf16(case.x)
+    q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    sm = torch.empty((M, K // 32), dtype=torch.uint8, device=dev)
+    for mode in ("floor", "rceil"):
+        med, mean = _time_calls(lambda: gq.mxfp8_dim0(x, mode, out=q, scales=sm), steps)
+        out[f"mxfp8_{mode}_{M}x{K}"] = rec(med, mean, 3 * M * K + M * K // 32,
+                                          l2="input larger than L2")
+    del x, q, sm
+    # stacked expert weights along dim1
+    E, Ke, Ne = EXPERT_SHAPE
+    rng = np.random.default_rng(1700)
+    w = rng.standard_normal((E, Ke, Ne), dtype=np.float32)
+    w *= np.power(np.float32(10), rng.uniform(-2, 2, size=(E, 1, Ne))).astype(np.float32)
+    wd = bf16(synth.to_bf16_bits(w))
+    del w
+    qe = torch.empty((E, Ke, Ne), dtype=torch.float8_e4m3fn, device=dev)
+    se = torch.empty((E, Ne), dtype=torch.float32, device=dev)
+    med, mean = _time_calls(lambda: gq.expert_dim1(wd, out=qe, scales=se), steps)
+    out[f"expert_dim1_{E}x{Ke}x{Ne}"] = rec(med, mean, 3 * E * Ke * Ne + 4 * E * Ne,
+                                            l2="input larger than L2")
+    del wd, qe
+    torch.cuda.empty_cache()
+    # the grouped grad_weight GEMM
+    T, N, K, G = WGRAD_SHAPE
+    rng = np.random.default_rng(1700)
+    c = synth.wgrad_case(T, N, K, synth.random_partition(rng, T, G), seed=1701)
+    d = lambda v: torch.from_numpy(v).to(dev)
+    qa, sa, qx, sx, offs = d(c.qa_t), d(c.sa), d(c.qx), d(c.sx), d(c.offs)
+    og = torch.empty((G, N, K), dtype=torch.bfloat16, device=dev)
+    med, mean = _time_calls(lambda: gq.grouped_wgrad(qa, sa, qx, sx, offs, out=og), 10)
+    flops = 2.0 * N * K * T
+    tf = flops / (med * 1e-6) / 1e12
+    sus, _ = measured_tensor_peak_fp8()
+    burst = 2.0 * measured_bf16_burst()
+    out[f"grouped_wgrad_T{T}_N{N}_K{K}_g{G}"] = {
+        "us": round(med, 1), "us_mean": round(mean, 1), "tflops": round(tf, 1),
+        "frac_of_sustained_fp8": round(tf / sus, 3), "frac_of_burst_fp8": round(tf / burst, 3),
+        "peak_note": "fp8 = measured bf16 x 2 (nominal fp8/bf16 ratio)"}
+    del qa, qx, og
+    torch.cuda.empty_cache()
+    gq.check_device_error()
+    return out
+
+
+def measured_bf16_burst():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
+
+
 def measured_tensor_peak_fp8():
     """fp8 dense peak for a kernel timed inside a sustained run (the timed
     calls follow seconds of the same load, under the power cap): the measured
@@ -516,6 +656,64 @@ def measured_tensor_peak_fp8():
                     "measured sustained bf16 x 2 (nominal fp8/bf16)")
     except (OSError, KeyError, ValueError):
         return 2.0 * 1700.0, "fallback sustained bf16 x 2 (nominal fp8/bf16)"
+
+
+def run_only(args):
+    """Times one kernel alone on its benchmark workload, launched back to
+    back on the stream (--only colwise | rowwise_t).  For profiling: in the
+    middle of a run of identical launches, the output lines a launch leaves
+    dirty in L2 are written back during the next, which leaves as many of
+    its own behind, so one launch's DRAM counters count one output."""
+    import numpy as np
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import fp8_quantization_moe_gb300 as gq
+    from fp8_quantization_moe_gb300 import synth
+
+    if args.only == "colwise":
+        M, K, G = COLWISE_SHAPE
+        case = synth.colwise_large(G, rows=M, cols=K)
+        nbytes = colwise_bytes(M, K, G)
+        x = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).to(dev)
+        o = torch.from_numpy(case.offs).to(dev)
+        q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+        sc = torch.empty((G, K), dtype=torch.float32, device=dev)
+        call = lambda: gq.colwise(x, o, out=q, scales=sc, pow2_scales=POW2)
+        workload = f"colwise X {M}x{K} bf16, {G} groups"
+    else:
+        N, Mg, G = ROWWISE_SHAPE
+        case = synth.rowwise_outliers(G, N=N, Mg=Mg)
+        nbytes = rowwise_bytes(N, Mg, G)
+        a = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).to(dev)
+        o = torch.from_numpy(case.offs).to(dev)
+        qt = torch.empty((Mg, N), dtype=torch.float8_e4m3fn, device=dev)
+        sc = torch.empty((N, G), dtype=torch.float32, device=dev)
+        call = lambda: gq.rowwise_t(a, o, out=qt, scales=sc, pow2_scales=POW2)
+        workload = f"rowwise_t A {N}x{Mg} bf16, {G} groups"
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record()
+    for i in range(args.steps):
+        call()
+        ev[i + 1].record()
+    torch.cuda.synchronize(dev)
+    gq.check_device_error()
+    per = [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(args.steps)]
+    peak, peak_kind = measured_peaks()
+    us = statistics.median(per)
+    print(json.dumps({"only": args.only, "workload": workload, "us_median": us,
+                      "gbs": nbytes / (us * 1e-6) / 1e9,
+                      "frac": nbytes / (us * 1e-6) / 1e9 / peak, "peak_kind": peak_kind,
+                      "steps": args.steps, "warmup": args.warmup,
+                      "gpu_launches": args.steps}), flush=True)
+    return 0
 
 
 def run_mine(args):
@@ -683,6 +881,10 @@ def run_mine(args):
             torch.distributed.destroy_process_group()
         return 0
 
+    per_config = None
+    if world == 1 and not args.no_per_config:
+        per_config = per_config_block(dev)
+
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         gbs, secs, sample = oracle_sample_gbs()
@@ -737,6 +939,7 @@ def run_mine(args):
             "traffic": (tr_row["dram_bytes_per_launch"] if tr_row else None),
             "algorithmic_bytes": row_b,
         },
+        "per_config": per_config,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_bytes / (e2e_max * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -763,6 +966,9 @@ def main(argv=None):
     ap.add_argument("--clock-window", type=float, default=1.5,
                     help="seconds of sustained load around the timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration block (every workload and group "
+                         "count, mxfp8, expert dim1 and the grouped GEMM, each timed alone)")
     ap.add_argument("--pow2-scales", action="store_true",
                     help="round every scale down to a power of two (the "
                          "round_scales_to_power_of_2 option); same bytes moved")
@@ -776,6 +982,9 @@ def main(argv=None):
                     help="time the grouped fp8 grad_weight GEMM instead of the main step")
     ap.add_argument("--wgrad-shape", default=None,
                     help="T,N,K,groups for --wgrad (a smaller case for profiling)")
+    ap.add_argument("--only", choices=["colwise", "rowwise_t"], default=None,
+                    help="time one kernel alone on its benchmark workload, launched "
+                         "back to back (for profiling)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time stream launches only (default: the step's two calls "
                          "replayed from CUDA graphs, stream launches reported beside)")
@@ -800,6 +1009,8 @@ def main(argv=None):
         return run_mxfp8(args)
     if args.wgrad:
         return run_wgrad(args)
+    if args.only:
+        return run_only(args)
     return run_mine(args)
 
 

@@ -20,7 +20,7 @@ token groups.  This package is argument marshalling over the library; torch
 supplies device memory and streams.  ``synth`` draws seeded inputs.
 """
 from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
-                       GQ_SCALE_POW2, GQ_WORKSPACE_ZEROED, GQError, check_device_error, colwise, colwise_host,
+                       GQ_SCALE_POW2, GQ_TWO_PHASE, GQ_WORKSPACE_ZEROED, GQError, check_device_error, colwise, colwise_host,
                        colwise_noalloc, expert_dim1, mxfp8_dim0,
                        grouped_wgrad, debug_set, lib, library_path, rowwise_t,
                        rowwise_t_host, set_lag, status_string, version,
@@ -28,7 +28,8 @@ from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
 from ._build import build
 
 __all__ = [
-    "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQ_SCALE_POW2", "GQ_WORKSPACE_ZEROED", "GQError",
+    "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQ_SCALE_POW2", "GQ_TWO_PHASE",
+    "GQ_WORKSPACE_ZEROED", "GQError",
     "build", "check_device_error", "colwise", "colwise_host",
     "colwise_noalloc", "debug_set", "expert_dim1", "grouped_wgrad", "mxfp8_dim0",
     "lib", "library_path", "rowwise_t", "rowwise_t_host", "set_lag",

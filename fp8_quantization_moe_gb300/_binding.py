@@ -25,6 +25,7 @@ GQ_KIND_ROWWISE_T = 1
 GQ_MAX_GROUPS = 1024
 GQ_SCALE_POW2 = 1
 GQ_WORKSPACE_ZEROED = 2
+GQ_TWO_PHASE = 4
 GQ_MX_FLOOR = 0
 GQ_MX_RCEIL = 1
 
@@ -166,11 +167,13 @@ def _check_in(x, offs, name):
 # ---------------------------------------------------------------- paths --
 
 def colwise(x: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
-            stream=None, workspace=None, pow2_scales: bool = False):
+            stream=None, workspace=None, pow2_scales: bool = False,
+            two_phase: bool = False):
     """Colwise per-token-group scaling (groups along dim0).
 
     ``pow2_scales`` rounds every scale down to a power of two
-    (GQ_SCALE_POW2).
+    (GQ_SCALE_POW2); ``two_phase`` sends every strip through the two-phase
+    path (GQ_TWO_PHASE; same results).
 
     x: bf16 (M, K) CUDA tensor; offs: int32 (n_groups,) end offsets on the
     same device.  Returns (q float8_e4m3fn (M, K), scales float32
@@ -192,7 +195,7 @@ def colwise(x: torch.Tensor, offs: torch.Tensor, *, out=None, scales=None,
         raise ValueError("colwise: scales must be a contiguous float32 (G, K) tensor")
     sh = _stream_handle(stream, dev)
     need = workspace_bytes(GQ_KIND_COLWISE, M, K, G)
-    flags = GQ_SCALE_POW2 if pow2_scales else 0
+    flags = (GQ_SCALE_POW2 if pow2_scales else 0) | (GQ_TWO_PHASE if two_phase else 0)
     if workspace is None:
         ws, zeroed = _workspace(need, dev, sh, GQ_KIND_COLWISE)
         flags |= GQ_WORKSPACE_ZEROED if zeroed else 0

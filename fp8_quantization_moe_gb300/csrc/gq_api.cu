@@ -175,8 +175,9 @@ using namespace gq;
 
 namespace {
 
-// every call that takes a workspace knows both flags
-constexpr uint32_t kKnownFlags = GQ_SCALE_POW2 | GQ_WORKSPACE_ZEROED;
+// the calls that take a workspace
+constexpr uint32_t kRowwiseFlags = GQ_SCALE_POW2 | GQ_WORKSPACE_ZEROED;
+constexpr uint32_t kColwiseFlags = kRowwiseFlags | GQ_TWO_PHASE;
 
 gq_status validate_common(const void* in, const void* out, const int32_t* offs,
                           int32_t n_groups, const float* scales, int64_t rows,
@@ -249,8 +250,8 @@ gq_status gq_fp8_colwise_ex(const void* x, int64_t M, int64_t K,
                             float* scales, uint32_t flags, void* workspace,
                             size_t workspace_bytes, gq_stream_t stream) {
   const char* name = "gq_fp8_colwise";
-  if (flags & ~kKnownFlags)
-    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kKnownFlags);
+  if (flags & ~kColwiseFlags)
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kColwiseFlags);
   gq_status st = validate_common(x, out, offs, n_groups, scales, M, K, name);
   if (st != GQ_OK) return st;
   if (K % 16 != 0)
@@ -277,8 +278,8 @@ gq_status gq_fp8_expert_dim1(const void* w, int64_t E, int64_t K, int64_t N, voi
                              float* scales, uint32_t flags, void* workspace,
                              size_t workspace_bytes, gq_stream_t stream) {
   const char* name = "gq_fp8_expert_dim1";
-  if (flags & ~kKnownFlags)
-    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kKnownFlags);
+  if (flags & ~kColwiseFlags)
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kColwiseFlags);
   if (E < 1 || K < 0 || N < 0)
     return fail(GQ_ERR_INVALID_ARG, "%s: bad sizes (%lld, %lld, %lld)", name,
                 static_cast<long long>(E), static_cast<long long>(K),
@@ -328,8 +329,8 @@ gq_status gq_fp8_rowwise_t_ex(const void* a, int64_t N, int64_t Mg,
                               float* scales, uint32_t flags, void* workspace,
                               size_t workspace_bytes, gq_stream_t stream) {
   const char* name = "gq_fp8_rowwise_t";
-  if (flags & ~kKnownFlags)
-    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kKnownFlags);
+  if (flags & ~kRowwiseFlags)
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags & ~kRowwiseFlags);
   gq_status st = validate_common(a, out_t, offs, n_groups, scales, N, Mg, name);
   if (st != GQ_OK) return st;
   if (N % 16 != 0)

@@ -29,7 +29,9 @@
 // never waits for other blocks, except that an item may not start before
 // the phase-B tiles up to `limit` tiles behind it have been taken -- the
 // phase-A data in flight, and so what L2 must hold until phase B re-reads
-// it, stays bounded; `limit` exceeds the longest strip's tile count, so the
+// it, stays bounded (`limit`: the longest strip's tile count plus 2.5 slabs
+// of phase-B tiles, or 1.25 tiles per block if that is more); `limit`
+// exceeds the longest strip's tile count, so the
 // strips of those phase-B tiles precede the item and are all claimed, and
 // the wait always ends.  Phase B waits only for strips whose phase-A tiles
 // are all claimed (all blocks are resident: the launch is cooperative), so
@@ -170,8 +172,9 @@ struct Params {
   uint64_t timeout_ns;
   uint64_t clear_words;  // 32-bit words from `strip` to the end of the workspace
   int32_t skip_arrival;
-  bool pow2;      // scales rounded down to powers of two
-  bool scales16;  // the scales base is 16-byte aligned (rows are: K % 16 == 0)
+  bool pow2;       // scales rounded down to powers of two
+  bool scales16;   // the scales base is 16-byte aligned (rows are: K % 16 == 0)
+  bool two_phase;  // no resident strips (GQ_TWO_PHASE)
 };
 
 // Four scales of one row of the (G, K) scale matrix, at a column that is a
@@ -226,7 +229,7 @@ __device__ __forceinline__ void build_plan(Smem& s, const Params& p, int lane) {
     if (g < p.G) {
       const int32_t rows = s.ends[g] - (g ? s.ends[g - 1] : 0);
       const int32_t nt = (rows + kTileRows - 1) / kTileRows;
-      const bool resident = rows <= kResRows;
+      const bool resident = rows <= kResRows && !p.two_phase;
       items = resident ? (rows > 0 ? 1 : 0) : nt;
       bt = resident ? 0 : nt;
     }
@@ -254,8 +257,14 @@ __device__ __forceinline__ void build_plan(Smem& s, const Params& p, int lane) {
     s.ip[p.G] = ci;
     s.bp[p.G] = cb;
     const int32_t nsl = (p.K + kW - 1) / kW;
+    // the lead: kLeadQuarters / 4 slabs of phase-B tiles, but never less
+    // than about one tile per block in flight, which phase one needs to keep
+    // every block busy (a slab of few tiles -- few rows, or uniform groups --
+    // would otherwise starve it)
     const int64_t quarters = p.forced_lag > 0 ? 4 * static_cast<int64_t>(p.forced_lag) : kLeadQuarters;
-    int64_t limit = static_cast<int64_t>(maxnt) + quarters * cb / 4;
+    int64_t lead = quarters * cb / 4;
+    if (p.forced_lag <= 0) lead = max(lead, (5 * static_cast<int64_t>(gridDim.x)) / 4);
+    int64_t limit = static_cast<int64_t>(maxnt) + lead;
     if (limit > (int64_t(1) << 30)) limit = int64_t(1) << 30;
     s.plan.nsl = nsl;
     s.plan.ts = ci;
@@ -849,6 +858,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   p.skip_arrival = dbg.skip_arrival;
   p.pow2 = (flags & GQ_SCALE_POW2) != 0;
   p.scales16 = (reinterpret_cast<uintptr_t>(scales) & 15) == 0;
+  p.two_phase = (flags & GQ_TWO_PHASE) != 0;
 
   const int64_t max_ctas = static_cast<int64_t>(info.sm_count) * info.colwise_ctas_per_sm;
   const int grid = static_cast<int>(items < max_ctas ? items : max_ctas);

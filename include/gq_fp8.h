@@ -162,6 +162,16 @@ gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,
  *                  per call).
  */
 #define GQ_WORKSPACE_ZEROED 2u
+/*
+ *   GQ_TWO_PHASE   (colwise and expert_dim1 only; GQ_ERR_INVALID_ARG for
+ *                  rowwise_t) every (group, 128-column slab) strip goes
+ *                  through the two-phase path -- amax tiles, then a second
+ *                  read for the cast -- also strips of at most 256 rows,
+ *                  which are otherwise loaded once and cast out of shared
+ *                  memory.  Results are identical; the option exists to
+ *                  test and time the two-phase path on any shape.
+ */
+#define GQ_TWO_PHASE 4u
 
 /*
  * gq_fp8_colwise / gq_fp8_rowwise_t with option flags; the calls above are

@@ -37,11 +37,12 @@ def dev_i32(a) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
 
 
-def run_colwise(gq, x_bits, offs, fill=SENTINEL, pow2=False):
+def run_colwise(gq, x_bits, offs, fill=SENTINEL, pow2=False, two_phase=False):
     M, K = x_bits.shape
     out = torch.full((M, K), fill, dtype=torch.uint8, device="cuda")
     q, s = gq.colwise(dev_bf16(x_bits), dev_i32(offs),
-                      out=out.view(torch.float8_e4m3fn), pow2_scales=pow2)
+                      out=out.view(torch.float8_e4m3fn), pow2_scales=pow2,
+                      two_phase=two_phase)
     gq.check_device_error()
     return q.view(torch.uint8).cpu().numpy(), s.cpu().numpy()
 
@@ -69,8 +70,8 @@ def assert_same(q, s, rq, rs, what):
                              f"gpu {s[i]!r} oracle {rs[i]!r}")
 
 
-def check_colwise(gq, case, pow2=False):
-    q, s = run_colwise(gq, case.x, case.offs, pow2=pow2)
+def check_colwise(gq, case, pow2=False, two_phase=False):
+    q, s = run_colwise(gq, case.x, case.offs, pow2=pow2, two_phase=two_phase)
     fill = np.full(case.x.shape, SENTINEL, np.uint8)
     rq, rs = oracle.colwise(case.x, case.offs, out=fill, pow2=pow2)
     assert_same(q, s, rq, rs, case.name)
@@ -112,10 +113,14 @@ ROWWISE_CASES = [
 
 
 @pytest.mark.parametrize("spec", COLWISE_CASES, ids=lambda s: f"{s[0]}x{s[1]}g{s[2]}")
-def test_colwise_small(gq, spec):
+@pytest.mark.parametrize("two_phase", [False, True], ids=["auto", "two_phase"])
+def test_colwise_small(gq, spec, two_phase):
+    """Ragged cases, with the resident path where strips allow it and with
+    every strip forced through the two phases (GQ_TWO_PHASE)."""
     r, c, g, seed, ne, al, mix, unc = spec
     check_colwise(gq, synth.random_case("colwise", r, c, g, seed, n_empty=ne,
-                                        align=al, scale_mix=mix, uncovered=unc))
+                                        align=al, scale_mix=mix, uncovered=unc),
+                  two_phase=two_phase)
 
 
 @pytest.mark.parametrize("spec", ROWWISE_CASES, ids=lambda s: f"{s[0]}x{s[1]}g{s[2]}")
@@ -235,13 +240,34 @@ def test_rowwise_resident_and_long_units(gq, widths, lead):
                                  "rowwise_t", base.x, offs, 0))
 
 
+@pytest.mark.parametrize("widths,K", [
+    ((255, 256, 257, 1, 16, 0, 300), 400),            # around the resident limit
+    ((767, 768, 769, 1536, 1537, 40), 272),           # around the tile size
+    ((256, 3000, 128, 0, 2305, 255, 17, 768), 1040),  # resident and long strips alternate
+])
+def test_colwise_resident_and_two_phase_strips(gq, widths, K):
+    """Group strips of at most 256 rows are folded and cast by one block out
+    of shared memory; longer ones go through the two phases in 768-row
+    tiles.  Groups just inside and past both sizes, empty and one-row
+    groups, mixed in one call, over several column slabs (the last one
+    partial)."""
+    offs = np.cumsum(widths).astype(np.int32)
+    M = int(offs[-1]) + 5  # uncovered tail rows keep the sentinel
+    base = synth.random_case("colwise", M, K, 1, seed=310 + len(widths), scale_mix=True)
+    check_colwise(gq, synth.Case("strips_" + "_".join(map(str, widths)), "colwise",
+                                 base.x, offs, 0))
+    check_colwise(gq, synth.Case("strips_pow2", "colwise", base.x, offs, 0), pow2=True)
+
+
 def test_short_super_tiles_many_tickets(gq):
-    """Token extents that end in a short super tile (fewer stages than
-    consumer warps), with several super tiles per CTA: warps that have no
-    stage in a super tile must still read its ticket before releasing its
-    context.  320 tokens = one full super tile of 256 + one of 64."""
-    check_colwise(gq, synth.random_case("colwise", 320, 65536, 5, seed=81,
-                                        n_empty=1, align=1, scale_mix=True))
+    """Many short pieces of work: 512 column slabs of five short strips
+    (colwise), or 1024 row bands of short groups (rowwise_t), so that every
+    block takes many items whose stages do not reach every consumer warp --
+    a warp must still read each context before releasing it."""
+    c = synth.random_case("colwise", 320, 65536, 5, seed=81, n_empty=1, align=1,
+                          scale_mix=True)
+    check_colwise(gq, c)
+    check_colwise(gq, c, two_phase=True)
     check_rowwise(gq, synth.random_case("rowwise_t", 65536, 320, 5, seed=82,
                                         n_empty=1, align=1, scale_mix=True))
 

@@ -1,19 +1,20 @@
 """The five workloads at full size, in the launch configuration the benchmark
 times (needs an sm_103 GPU).
 
-The two small workloads are compared with the oracle in full.  The large
-ones are compared on sampled outputs the oracle computes exactly -- whole
-column slabs / row bands at both ends plus random columns / rows (a column of
-colwise, or a row of rowwise_t, depends on nothing else) -- and checked at
-full size against properties that hold at any size: every group column (or
-row) with amax >= 1e-12 holds a +-448 code, no NaN code appears, and
-rowwise_t(A) equals colwise(A^T) with transposed scales.
+Every workload -- 1 and 2, 3 at 4, 8 and 16 groups, 4, and 5 at 1 and 64
+groups -- is compared with the oracle in full: every fp8 byte and every
+fp32 scale bit pattern, with untouched bytes keeping a sentinel.  The large
+ones run the oracle over the host's cores in independent column (colwise)
+or row (rowwise_t) slices.  On top, properties that hold at any size: every
+group column (or row) with amax >= 1e-12 holds a +-448 code, no NaN code
+appears, and rowwise_t(A) equals colwise(A^T) with transposed scales.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
+import oracle_parallel
 from fp8_quantization_moe_gb300 import synth
 from test_gpu_parity import (SENTINEL, assert_same, check_colwise,
                              check_rowwise, dev_bf16, dev_i32)
@@ -29,13 +30,6 @@ def gq():
     import fp8_quantization_moe_gb300 as m
 
     return m
-
-
-def _sample(rng, extent, tile, n_random):
-    idx = set(range(min(tile, extent)))
-    idx |= set(range(max(0, extent - tile), extent))
-    idx |= set(rng.choice(extent, size=min(n_random, extent), replace=False).tolist())
-    return np.array(sorted(idx))
 
 
 def _max_code_property(q_dev: torch.Tensor, x_dev: torch.Tensor, offs, dim):
@@ -67,35 +61,32 @@ def test_small_workloads_full(gq, idx):
 
 @pytest.mark.parametrize("n_groups", [4, 8, 16])
 def test_colwise_large(gq, n_groups):
+    """Workload 3 in full: X (65536, 4096) at 4, 8 and 16 groups."""
     case = synth.workload(3, n_groups)
     x = dev_bf16(case.x)
     offs = dev_i32(case.offs)
-    q, s = gq.colwise(x, offs)
+    out = torch.full(case.x.shape, SENTINEL, dtype=torch.uint8, device="cuda")
+    q, s = gq.colwise(x, offs, out=out.view(torch.float8_e4m3fn))
     gq.check_device_error()
-    rng = np.random.default_rng(100 + n_groups)
-    cols = _sample(rng, case.x.shape[1], 128, 64)
-    rq, rs = oracle.colwise(case.x[:, cols], case.offs)
-    cols_d = torch.from_numpy(cols).cuda()
-    gq_q = q.view(torch.uint8).index_select(1, cols_d).cpu().numpy()
-    gq_s = s.index_select(1, cols_d).cpu().numpy()
-    assert_same(gq_q, gq_s, rq, rs, case.name)
+    rq, rs = oracle_parallel.colwise(case.x, case.offs,
+                                     out=np.full(case.x.shape, SENTINEL, np.uint8))
+    assert_same(q.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), rq, rs, case.name)
     _max_code_property(q, x, case.offs, 0)
 
 
 @pytest.mark.parametrize("idx,n_groups", [(4, 16), (5, 1), (5, 64)])
 def test_rowwise_large(gq, idx, n_groups):
+    """Workloads 4 and 5 in full: A (8192, 16640) at 16, 1 and 64 groups."""
     case = synth.workload(idx, n_groups)
     a = dev_bf16(case.x)
     offs = dev_i32(case.offs)
-    qt, s = gq.rowwise_t(a, offs)
+    N, Mg = case.x.shape
+    out = torch.full((Mg, N), SENTINEL, dtype=torch.uint8, device="cuda")
+    qt, s = gq.rowwise_t(a, offs, out=out.view(torch.float8_e4m3fn))
     gq.check_device_error()
-    rng = np.random.default_rng(200 + n_groups)
-    rows = _sample(rng, case.x.shape[0], 128, 64)
-    rq, rs = oracle.rowwise_t(case.x[rows], case.offs)
-    rows_d = torch.from_numpy(rows).cuda()
-    gq_q = qt.view(torch.uint8).index_select(1, rows_d).cpu().numpy()
-    gq_s = s.index_select(0, rows_d).cpu().numpy()
-    assert_same(gq_q, gq_s, rq, rs, case.name)
+    rq, rs = oracle_parallel.rowwise_t(case.x, case.offs,
+                                       out=np.full((Mg, N), SENTINEL, np.uint8))
+    assert_same(qt.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), rq, rs, case.name)
     _max_code_property(qt, a, case.offs, 1)
     # the transpose identity at full size: rowwise_t(A) == colwise(A^T)
     qc, sc = gq.colwise(a.t().contiguous(), offs)
@@ -105,33 +96,27 @@ def test_rowwise_large(gq, idx, n_groups):
 
 
 def test_pow2_scales_full_size(gq):
-    """The two benchmark workloads with power-of-two scales, on sampled
-    columns / rows the oracle computes exactly."""
+    """The two benchmark workloads with power-of-two scales, in full."""
     case = synth.workload(3, 16)
     x, offs = dev_bf16(case.x), dev_i32(case.offs)
     q, s = gq.colwise(x, offs, pow2_scales=True)
     gq.check_device_error()
-    rng = np.random.default_rng(500)
-    cols = _sample(rng, case.x.shape[1], 128, 48)
-    rq, rs = oracle.colwise(case.x[:, cols], case.offs, pow2=True)
-    cols_d = torch.from_numpy(cols).cuda()
-    assert_same(q.view(torch.uint8).index_select(1, cols_d).cpu().numpy(),
-                s.index_select(1, cols_d).cpu().numpy(), rq, rs, case.name + "_pow2")
+    rq, rs = oracle_parallel.colwise(case.x, case.offs, pow2=True)
+    assert_same(q.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), rq, rs,
+                case.name + "_pow2")
     del x, q, s
     case = synth.workload(5, 64)
     a, offs = dev_bf16(case.x), dev_i32(case.offs)
     qt, s = gq.rowwise_t(a, offs, pow2_scales=True)
     gq.check_device_error()
-    rows = _sample(rng, case.x.shape[0], 128, 48)
-    rq, rs = oracle.rowwise_t(case.x[rows], case.offs, pow2=True)
-    rows_d = torch.from_numpy(rows).cuda()
-    assert_same(qt.view(torch.uint8).index_select(1, rows_d).cpu().numpy(),
-                s.index_select(0, rows_d).cpu().numpy(), rq, rs, case.name + "_pow2")
+    rq, rs = oracle_parallel.rowwise_t(case.x, case.offs, pow2=True)
+    assert_same(qt.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), rq, rs,
+                case.name + "_pow2")
 
 
 def test_expert_dim1_full_size(gq):
     """Eight experts of (4096, 4096) bf16 weights -- 256 MB, larger than L2 --
-    on sampled columns, which the oracle computes exactly."""
+    in full."""
     rng = np.random.default_rng(601)
     E, K, N = 8, 4096, 4096
     x = rng.standard_normal((E, K, N), dtype=np.float32)
@@ -141,23 +126,18 @@ def test_expert_dim1_full_size(gq):
     wd = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).cuda()
     q, s = gq.expert_dim1(wd)
     gq.check_device_error()
-    cols = _sample(rng, N, 128, 48)
-    rq, rs = oracle.expert_dim1(np.ascontiguousarray(w[:, :, cols]))
-    cols_d = torch.from_numpy(cols).cuda()
-    assert_same(q.view(torch.uint8).index_select(2, cols_d).cpu().numpy(),
-                s.index_select(1, cols_d).cpu().numpy(), rq, rs, "expert_dim1_8x4096x4096")
+    rq, rs = oracle_parallel.expert_dim1(w)
+    assert_same(q.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), rq, rs,
+                "expert_dim1_8x4096x4096")
 
 
 @pytest.mark.parametrize("mode", ["floor", "rceil"])
 def test_mxfp8_full_size(gq, mode):
-    """The colwise benchmark input X (65536, 4096) through the mxfp8 cast, on
-    sampled rows (the cast is row-local, so the oracle computes them exactly)."""
+    """The colwise benchmark input X (65536, 4096) through the mxfp8 cast, in
+    full."""
     case = synth.workload(3, 16)
     q, s = gq.mxfp8_dim0(dev_bf16(case.x), mode)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(701)
-    rows = _sample(rng, case.x.shape[0], 64, 64)
-    rq, rs = oracle.mxfp8_dim0(np.ascontiguousarray(case.x[rows]), 0 if mode == "floor" else 1)
-    rows_d = torch.from_numpy(rows).cuda()
-    assert np.array_equal(s.index_select(0, rows_d).cpu().numpy(), rs)
-    assert np.array_equal(q.view(torch.uint8).index_select(0, rows_d).cpu().numpy(), rq)
+    rq, rs = oracle_parallel.mxfp8_dim0(case.x, 0 if mode == "floor" else 1)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.view(torch.uint8).cpu().numpy(), rq)

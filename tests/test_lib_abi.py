@@ -142,9 +142,10 @@ def test_ex_calls_reject_unknown_flags(gq):
     lib = gq.lib()
     assert gq.GQ_SCALE_POW2 == 1
     assert gq.GQ_WORKSPACE_ZEROED == 2
-    for bad in (4, 0x80000000, 7):
+    assert gq.GQ_TWO_PHASE == 4
+    for bad in (8, 0x80000000, 15):
         assert lib.gq_fp8_colwise_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1
-    for bad in (4, 0x80000000, 7):
+    for bad in (4, 0x80000000, 7):   # GQ_TWO_PHASE is colwise's alone
         assert lib.gq_fp8_rowwise_t_ex(A16, 16, 16, A16, 1, A16, A16, bad, A16, 1 << 20, None) == 1
 
 
@@ -154,7 +155,7 @@ def test_ex_calls_reject_unknown_flags(gq):
     ((A16, 2000, 16, 16, A16, A16, 0, A16, 1 << 20), 2),   # > GQ_MAX_GROUPS
     ((A16, 2, 16, 24, A16, A16, 0, A16, 1 << 20), 2),      # N % 16
     ((A16, 2, -1, 16, A16, A16, 0, A16, 1 << 20), 1),      # negative K
-    ((A16, 2, 16, 16, A16, A16, 4, A16, 1 << 20), 1),      # unknown flag
+    ((A16, 2, 16, 16, A16, A16, 8, A16, 1 << 20), 1),      # unknown flag
     ((A16, 2, 16, 16, None, A16, 0, A16, 1 << 20), 1),     # NULL output
     ((A16, 2, 16, 16, A16, A16, 0, A16, 100), 1),          # workspace too small
     ((A16, 4, 1 << 30, 16, A16, A16, 0, A16, 1 << 20), 2),  # E * K >= 2^31
