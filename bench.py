@@ -660,10 +660,12 @@ def measured_tensor_peak_fp8():
 
 def run_only(args):
     """Times one kernel alone on its benchmark workload, launched back to
-    back on the stream (--only colwise | rowwise_t).  For profiling: in the
-    middle of a run of identical launches, the output lines a launch leaves
-    dirty in L2 are written back during the next, which leaves as many of
-    its own behind, so one launch's DRAM counters count one output."""
+    back on the stream (--only colwise | rowwise_t), the outputs alternating
+    between two buffers.  For profiling: in the middle of such a run, the
+    output lines a launch leaves dirty in L2 are written back during the
+    next, which leaves as many of its own behind (to other addresses, so
+    none is merged with a later write), and one launch's DRAM counters count
+    one output."""
     import numpy as np
     import torch
 
@@ -681,9 +683,9 @@ def run_only(args):
         nbytes = colwise_bytes(M, K, G)
         x = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).to(dev)
         o = torch.from_numpy(case.offs).to(dev)
-        q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
-        sc = torch.empty((G, K), dtype=torch.float32, device=dev)
-        call = lambda: gq.colwise(x, o, out=q, scales=sc, pow2_scales=POW2)
+        qs = [torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev) for _ in range(2)]
+        ss = [torch.empty((G, K), dtype=torch.float32, device=dev) for _ in range(2)]
+        call = lambda i: gq.colwise(x, o, out=qs[i % 2], scales=ss[i % 2], pow2_scales=POW2)
         workload = f"colwise X {M}x{K} bf16, {G} groups"
     else:
         N, Mg, G = ROWWISE_SHAPE
@@ -691,17 +693,17 @@ def run_only(args):
         nbytes = rowwise_bytes(N, Mg, G)
         a = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).to(dev)
         o = torch.from_numpy(case.offs).to(dev)
-        qt = torch.empty((Mg, N), dtype=torch.float8_e4m3fn, device=dev)
-        sc = torch.empty((N, G), dtype=torch.float32, device=dev)
-        call = lambda: gq.rowwise_t(a, o, out=qt, scales=sc, pow2_scales=POW2)
+        qs = [torch.empty((Mg, N), dtype=torch.float8_e4m3fn, device=dev) for _ in range(2)]
+        ss = [torch.empty((N, G), dtype=torch.float32, device=dev) for _ in range(2)]
+        call = lambda i: gq.rowwise_t(a, o, out=qs[i % 2], scales=ss[i % 2], pow2_scales=POW2)
         workload = f"rowwise_t A {N}x{Mg} bf16, {G} groups"
-    for _ in range(args.warmup):
-        call()
+    for i in range(args.warmup):
+        call(i)
     torch.cuda.synchronize(dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     ev[0].record()
     for i in range(args.steps):
-        call()
+        call(args.warmup + i)
         ev[i + 1].record()
     torch.cuda.synchronize(dev)
     gq.check_device_error()

@@ -12,7 +12,8 @@
 // strip alone.  A strip of at most kResRows = 256 rows is "resident": one
 // block loads it once, folds its column maxima, computes its scales and
 // casts it out of shared memory (one HBM read, no other block involved).  A
-// longer strip is cut into tiles of kTileRows = 768 rows (the last one
+// longer strip is cut into tiles of kTileRows = 768 rows (fewer for small
+// problems, so that every block gets several; the last tile of a strip
 // shorter) and goes through two phases:
 //   phase A -- a block folds a tile's column maxima, adds them to the
 //     strip's amax words in global memory (one atomicMax per column) and
@@ -34,8 +35,9 @@
 // exceeds the longest strip's tile count, so the
 // strips of those phase-B tiles precede the item and are all claimed, and
 // the wait always ends.  Phase B waits only for strips whose phase-A tiles
-// are all claimed (all blocks are resident: the launch is cooperative), so
-// every wait ends.
+// are all claimed.  Claims are made by running blocks, in order, and each
+// block works through its claims in order, so every wait ends whichever
+// blocks are resident (the launch needs no co-residency).
 //
 // Block roles (18 warps).  Phase one: a scheduler warp claims items (one
 // ahead) and publishes a context per item in a ring of four -- few, so
@@ -67,8 +69,8 @@ namespace gq {
 namespace colwise {
 
 constexpr int kRows = 32;                       // rows per stage (one TMA box)
-constexpr int kTileStages = 24;                 // stages per two-phase tile
-constexpr int kTileRows = kTileStages * kRows;  // rows per two-phase tile
+constexpr int kTileStages = 24;                 // stages per two-phase tile (at most)
+constexpr int kTileRows = kTileStages * kRows;  // rows per two-phase tile (at most)
 constexpr int kResStages = 8;                   // a strip of up to this many stages is resident
 constexpr int kResRows = kResStages * kRows;
 constexpr int kStages = 12;                     // stage ring of each pipeline
@@ -168,6 +170,7 @@ struct Params {
   float* scales;
   unsigned* err;
   int32_t M, K, G;
+  int32_t tile_rows;   // rows per two-phase tile: kTileRows, or less for small problems
   int32_t forced_lag;  // > 0: the phase-A lead in slabs of phase-B tiles
   uint64_t timeout_ns;
   uint64_t clear_words;  // 32-bit words from `strip` to the end of the workspace
@@ -228,7 +231,7 @@ __device__ __forceinline__ void build_plan(Smem& s, const Params& p, int lane) {
     int32_t items = 0, bt = 0;
     if (g < p.G) {
       const int32_t rows = s.ends[g] - (g ? s.ends[g - 1] : 0);
-      const int32_t nt = (rows + kTileRows - 1) / kTileRows;
+      const int32_t nt = (rows + p.tile_rows - 1) / p.tile_rows;
       const bool resident = rows <= kResRows && !p.two_phase;
       items = resident ? (rows > 0 ? 1 : 0) : nt;
       bt = resident ? 0 : nt;
@@ -292,11 +295,11 @@ __device__ __forceinline__ int find_group(const int32_t* pre, int n, int32_t j, 
 }
 
 // The context fields of tile k of strip (g, d).
-__device__ __forceinline__ void fill_ctx(Ctx& c, const Smem& s, int32_t type, int g, int32_t d,
-                                         int32_t k, int32_t hold) {
+__device__ __forceinline__ void fill_ctx(Ctx& c, const Smem& s, int32_t tile_rows, int32_t type,
+                                         int g, int32_t d, int32_t k, int32_t hold) {
   const int32_t sg = g ? s.ends[g - 1] : 0;
-  const int32_t row0 = sg + k * kTileRows;
-  const int32_t rows = min(kTileRows, s.ends[g] - row0);
+  const int32_t row0 = sg + k * tile_rows;
+  const int32_t rows = min(tile_rows, s.ends[g] - row0);
   c.type = type;
   c.g = g;
   c.d = d;
@@ -304,7 +307,7 @@ __device__ __forceinline__ void fill_ctx(Ctx& c, const Smem& s, int32_t type, in
   c.row0 = row0;
   c.rows = rows;
   c.nsub = (rows + kRows - 1) / kRows;
-  c.ntiles = (s.ends[g] - sg + kTileRows - 1) / kTileRows;
+  c.ntiles = (s.ends[g] - sg + tile_rows - 1) / tile_rows;
   c.hold = hold;
   c.f_cnt = 0;
 }
@@ -356,7 +359,7 @@ __device__ __forceinline__ void sched_a(Smem& s, const Params& p, int lane) {
       }
     }
     if (lane == 0)
-      fill_ctx(c, s, resident ? kTypeR : kTypeA, g, static_cast<int32_t>(d), k,
+      fill_ctx(c, s, p.tile_rows, resident ? kTypeR : kTypeA, g, static_cast<int32_t>(d), k,
                p.skip_arrival && !resident && d == 0 && k == 0);
     sts128(smem_addr(&c.amax[4 * lane]), make_uint4(0, 0, 0, 0));
     __syncwarp();
@@ -694,7 +697,9 @@ __device__ __forceinline__ void scale_warp(Smem& s, const Params& p, int i, int 
     const uint32_t d = h / static_cast<uint32_t>(pl.tb);
     const uint32_t j = h - d * static_cast<uint32_t>(pl.tb);
     const int g = find_group(s.bp, p.G, static_cast<int32_t>(j), lane);
-    if (lane == 0) fill_ctx(c, s, kTypeB, g, static_cast<int32_t>(d), static_cast<int32_t>(j) - s.bp[g], 0);
+    if (lane == 0)
+      fill_ctx(c, s, p.tile_rows, kTypeB, g, static_cast<int32_t>(d), static_cast<int32_t>(j) - s.bp[g],
+               0);
     __syncwarp();
     // the tile is published (and loaded) only once its strip is complete:
     // loaded earlier, it could come from HBM ahead of phase A, and it would
@@ -852,6 +857,14 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   p.M = M;
   p.K = K;
   p.G = G;
+  // the largest tile that still gives every block about four tiles per phase
+  const int64_t max_ctas = static_cast<int64_t>(info.sm_count) * info.colwise_ctas_per_sm;
+  p.tile_rows = kResRows;
+  for (int32_t rows = kTileRows; rows > kResRows; rows -= kResRows)
+    if (((K + kW - 1) / kW) * static_cast<int64_t>(M) / rows >= 4 * max_ctas) {
+      p.tile_rows = rows;
+      break;
+    }
   p.forced_lag = dbg.lag[GQ_KIND_COLWISE];
   p.timeout_ns = dbg.timeout_ns;
   p.clear_words = (L.total - L.counters) / 4;
@@ -860,20 +873,17 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   p.scales16 = (reinterpret_cast<uintptr_t>(scales) & 15) == 0;
   p.two_phase = (flags & GQ_TWO_PHASE) != 0;
 
-  const int64_t max_ctas = static_cast<int64_t>(info.sm_count) * info.colwise_ctas_per_sm;
   const int grid = static_cast<int>(items < max_ctas ? items : max_ctas);
   if (!(flags & GQ_WORKSPACE_ZEROED)) {
     st = check_cuda(cudaMemsetAsync(ws, 0, L.total, stream), "colwise: clear workspace");
     if (st != GQ_OK) return st;
   }
-  // cooperative: phase B waits for phase A of other blocks, so every block
-  // must be resident
-  void* args[] = {&xmap, &p};
-  return check_cuda(
-      cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(colwise_kernel),
-                                  dim3(grid), dim3(kThreads), args, kSmemBytes,
-                                  stream),
-      "colwise: launch");
+  // A plain launch: blocks need not be resident together.  Every wait is on
+  // work that a running block has claimed -- items, tiles and phase-B reads
+  // are claimed from counters in order, and each block works through its
+  // claims in order -- so the kernel progresses whichever blocks run.
+  colwise_kernel<<<grid, kThreads, kSmemBytes, stream>>>(xmap, p);
+  return check_cuda(cudaGetLastError(), "colwise: launch");
 }
 
 }  // namespace colwise
