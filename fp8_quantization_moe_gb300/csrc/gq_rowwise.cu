@@ -25,7 +25,9 @@
 // from L2 where it can.
 //
 // A descriptor warp claims units and publishes each in a small ring of unit
-// descriptors; a loader warp follows the descriptors and issues the TMA
+// descriptors -- at most `lag` units in flight, about kBudget windows' worth
+// of the average unit, so that short units keep the consumers fed and long
+// ones do not pile up in the last claims --; a loader warp follows the descriptors and issues the TMA
 // loads of the block's window stream into a ring of kStages windows, kIssue
 // windows side by side.  Pass A of a unit folds its amax, pass B scales,
 // casts and stores it; a pass covers the unit's windows in order.  Resident
@@ -49,8 +51,9 @@
 //     chunk, ldmatrix.x4.trans gives lane l the pairs
 //     (n, n+1) of rows 8i + 2(l%4) of column 8c + l/4, which are multiplied
 //     in fp32 (mul.rn.f32x2) and packed with cvt.rn.satfinite.e4m3x2; a 4x4
-//     exchange of byte pairs among the four lanes of a column leaves each
-//     lane 8 consecutive bytes of a row of A^T, stored with one 8-byte store.
+//     exchange of words among the four lanes of a column, over both halves,
+//     leaves each lane 16 consecutive bytes of a row of A^T, stored with one
+//     16-byte store.
 // Every warp walks the same stream and derives each visit's ring slot from
 // the descriptors, so a window costs one barrier wait to read and one
 // arrival to release.
@@ -69,8 +72,9 @@ namespace rowwise {
 
 constexpr int kStages = 24;  // ring of windows
 constexpr int kFit = 12;     // windows a unit may keep resident between passes
-constexpr int kUnits = 4;    // unit descriptors in flight
-constexpr int kConsumerWarps = 8;
+constexpr int kUnits = 8;    // unit descriptors (at most in flight)
+constexpr int kBudget = 40;  // ring loads the units in flight should come to, about
+constexpr int kConsumerWarps = 10;
 constexpr int kAhead = 2;  // units a block claims before it needs them
 constexpr int kIssue = 8;  // producer lanes issuing window loads side by side
 constexpr int kLoaderWarp = kConsumerWarps;
@@ -80,6 +84,7 @@ constexpr int kQ = kTn / 32;  // 32-row halves of a window
 constexpr int kStageBytes = kTn * kTm * 2;
 static_assert(kTm * 2 == 128 && kTn == 64, "128-byte swizzled rows, two 32-row halves");
 static_assert(2 * kFit <= kStages, "the ring holds two consecutive resident units");
+static_assert(kUnits >= 2, "pass B of a resident unit follows pass A of the next");
 static_assert(kIssue <= kStages && kIssue <= 32, "a batch of loads takes distinct slots");
 
 struct Unit {
@@ -118,6 +123,7 @@ struct Params {
   int32_t N, Mg, G;
   uint32_t units;  // row bands x groups
   uint32_t bands;  // row bands of kTn rows
+  int32_t lag;     // units in flight per block (2 .. kUnits)
   uint64_t timeout_ns;
   int32_t skip_arrival;
   bool pow2;  // scales rounded down to powers of two
@@ -188,7 +194,13 @@ __device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int la
     const int32_t x0 = s0 & ~7;
     const int nst = n0 >= 0 ? (e0 - x0 + kTm - 1) / kTm : 0;
     const int us = static_cast<int>(useq % kUnits);
-    const bool ok = mbar_wait(&s.u_free[us], ((useq / kUnits) & 1) ^ 1u, wait_ns, p.err);
+    // at most p.lag units in flight: unit useq - lag must be finished (units
+    // finish in stream order), which also frees this descriptor
+    bool ok = true;
+    if (useq >= static_cast<uint32_t>(p.lag)) {
+      const uint32_t v = useq - static_cast<uint32_t>(p.lag);
+      ok = mbar_wait(&s.u_free[v % kUnits], (v / kUnits) & 1, wait_ns, p.err);
+    }
     if (__any_sync(0xffffffffu, !ok)) return;
     Unit& U = s.unit[us];
     if (lane < kTn / 4) sts128(smem_addr(&U.amax[4 * lane]), make_uint4(0, 0, 0, 0));
@@ -294,21 +306,27 @@ __device__ __forceinline__ void fold_a(Unit& U, int ca, int cb, uint32_t tile, i
 
 // B visit: scale, cast and transpose the window at token column xw (group
 // columns [ca, cb) of it); store rows of A^T.  scale[r] is the scale of row
-// n0 + r.  Each 32-row half goes through the steps in batches of
-// all eight 8-column chunks -- loads, casts, the two exchanges, stores -- so
-// that eight independent chains hide the latency of each step; chunks
-// outside [ca, cb) are computed from the window's other columns and not
-// stored.
+// n0 + r.  Both 32-row halves go through ldmatrix and the cast first, in
+// batches of all eight 8-column chunks, so that eight independent chains
+// hide the latency of each step; then, per chunk, a 4x4 exchange of words
+// among the four lanes of a column leaves each lane 16 consecutive bytes of
+// a row of A^T (rows 16 q .. 16 q + 15 of the band), stored with one 16-byte
+// store.  Chunks outside [ca, cb) are computed from the window's other
+// columns and not stored.
 __device__ __forceinline__ void quant_b(int32_t n0, int32_t xw, int ca, int cb,
                                         const float* scale, uint32_t tile, const Params& p,
                                         int lane) {
   const int q = lane & 3;
   const int mcol = lane >> 2;  // column within an 8-column chunk
-  // this lane's stores: bytes n0 + 32 i + 8 q .. + 7 of A^T rows
-  uint8_t* obase = p.out_t + static_cast<size_t>(xw + mcol) * p.N + n0 + 8 * q;
+  // this lane's stores: bytes n0 + 16 q .. + 15 of A^T rows
+  uint8_t* obase = p.out_t + static_cast<size_t>(xw + mcol) * p.N + n0 + 16 * q;
   const size_t N8 = 8 * static_cast<size_t>(p.N);
   const uint32_t lrow = tile + static_cast<uint32_t>(lane) * 128u;  // ldmatrix row address base
   constexpr int kC = kTm / 8;  // chunks
+  // w[cc][t]: the cast bytes of rows 16 t + (2q, 2q+1, 8+2q, 9+2q) of
+  // column 8 cc + mcol (t = 2 qq: matrices 0, 1 of half qq; t = 2 qq + 1:
+  // matrices 2, 3)
+  uint32_t w[kC][4];
 #pragma unroll
   for (int qq = 0; qq < kQ; ++qq) {
     // scales of rows 32 qq + 8 i + 2q (+1), the rows of matrix i
@@ -324,36 +342,39 @@ __device__ __forceinline__ void quant_b(int32_t n0, int32_t xw, int ca, int cb,
     for (int cc = 0; cc < kC; ++cc)
       ldsm_x4_trans(lrow + qq * 32 * 128 + ((((cc ^ lane) & 7)) << 4), r[cc][0], r[cc][1],
                     r[cc][2], r[cc][3]);
-    // p01: bytes of rows 2q, 2q+1 (matrix 0) and 8+2q, 9+2q (matrix 1);
-    // p23: matrices 2 and 3 -- the pairs V[q][i] of lane q
-    uint32_t p01[kC], p23[kC];
 #pragma unroll
     for (int cc = 0; cc < kC; ++cc) {
-      p01[cc] = quant4(r[cc][0], r[cc][1], sv[0], sv[1], sv[2], sv[3]);
-      p23[cc] = quant4(r[cc][2], r[cc][3], sv[4], sv[5], sv[6], sv[7]);
+      w[cc][2 * qq] = quant4(r[cc][0], r[cc][1], sv[0], sv[1], sv[2], sv[3]);
+      w[cc][2 * qq + 1] = quant4(r[cc][2], r[cc][3], sv[4], sv[5], sv[6], sv[7]);
     }
-    // 4x4 transpose of pairs among the lanes of one column: lane q ends
-    // with V[0][q], V[1][q], V[2][q], V[3][q] = rows 8q .. 8q + 7
-    uint32_t tlo[kC], thi[kC];
+  }
+  // lane q holds M[q][t] = w[.][t] for the four targets t; lane t needs
+  // M[0..3][t].  Step 1 (partner q ^ 2) swaps the two words whose target
+  // differs from q in bit 1, step 2 (partner q ^ 1) those differing in bit 0.
+  const bool b2 = (q & 2) != 0, b1 = (q & 1) != 0;
+  // byte order of the 16 rows: words of lanes (0, 1) give rows 0-3 (low
+  // halves) and 8-11 (high halves), lanes (2, 3) rows 4-7 and 12-15
+  const uint32_t sel_lo = b1 ? 0x1054u : 0x5410u;
+  const uint32_t sel_hi = b1 ? 0x3276u : 0x7632u;
+  const bool st_ok = n0 + 16 * q < p.N;
 #pragma unroll
-    for (int cc = 0; cc < kC; ++cc) {
-      const uint32_t x1 = __shfl_xor_sync(0xffffffffu, (q & 2) ? p01[cc] : p23[cc], 2);
-      tlo[cc] = (q & 2) ? x1 : p01[cc];
-      thi[cc] = (q & 2) ? p23[cc] : x1;
-    }
-    const bool st_ok = n0 + 32 * qq + 8 * q < p.N;
-#pragma unroll
-    for (int cc = 0; cc < kC; ++cc) {
-      const uint32_t x2 = __shfl_xor_sync(
-          0xffffffffu, __byte_perm(tlo[cc], thi[cc], (q & 1) ? 0x5410 : 0x7632), 1);
-      const uint32_t w0 =
-          (q & 1) ? __byte_perm(x2, tlo[cc], 0x7610) : __byte_perm(tlo[cc], x2, 0x5410);
-      const uint32_t w1 =
-          (q & 1) ? __byte_perm(x2, thi[cc], 0x7632) : __byte_perm(thi[cc], x2, 0x7610);
-      const int m = cc * 8 + mcol;  // window column
-      if (m >= ca && m < cb && st_ok)
-        __stcs(reinterpret_cast<uint2*>(obase + cc * N8 + qq * 32), make_uint2(w0, w1));
-    }
+  for (int cc = 0; cc < kC; ++cc) {
+    const uint32_t own0 = b2 ? w[cc][2] : w[cc][0];  // M[q][t0], t0 = q & 2
+    const uint32_t own1 = b2 ? w[cc][3] : w[cc][1];  // M[q][t0 + 1]
+    const uint32_t g0 = __shfl_xor_sync(0xffffffffu, b2 ? w[cc][0] : w[cc][2], 2);  // M[q^2][t0]
+    const uint32_t g1 = __shfl_xor_sync(0xffffffffu, b2 ? w[cc][1] : w[cc][3], 2);  // M[q^2][t0+1]
+    const uint32_t a = b1 ? own1 : own0;  // M[q][q]
+    const uint32_t c = b1 ? g1 : g0;      // M[q^2][q]
+    const uint32_t bb = __shfl_xor_sync(0xffffffffu, b1 ? own0 : own1, 1);  // M[q^1][q]
+    const uint32_t d = __shfl_xor_sync(0xffffffffu, b1 ? g0 : g1, 1);       // M[q^3][q]
+    // sources 0..3 are (a, bb, c, d) permuted by q: lanes (0,1) -> (P, Q),
+    // lanes (2, 3) -> (R, S), each pair swapped when q is odd (sel_*)
+    const uint32_t P = b2 ? c : a, Q = b2 ? d : bb, R = b2 ? a : c, S = b2 ? bb : d;
+    const int m = cc * 8 + mcol;  // window column
+    if (m >= ca && m < cb && st_ok)
+      __stcs(reinterpret_cast<uint4*>(obase + cc * N8),
+             make_uint4(__byte_perm(P, Q, sel_lo), __byte_perm(R, S, sel_lo),
+                        __byte_perm(P, Q, sel_hi), __byte_perm(R, S, sel_hi)));
   }
 }
 
@@ -578,6 +599,16 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
   p.G = G;
   p.units = static_cast<uint32_t>(units);
   p.bands = static_cast<uint32_t>(bands);
+  // units in flight: about kBudget ring loads' worth of the average unit (a
+  // long unit streams twice), at least two -- more overlap the short units'
+  // descriptor and scale waits, fewer keep the last claims of a grid with
+  // few units per block balanced
+  {
+    int64_t win = (Mg / G + kTm - 1) / kTm + 1;
+    if (win > kFit) win *= 2;
+    int64_t lag = kBudget / win;
+    p.lag = static_cast<int32_t>(lag < 2 ? 2 : lag > kUnits ? kUnits : lag);
+  }
   p.timeout_ns = dbg.timeout_ns;
   p.skip_arrival = dbg.skip_arrival;
   p.pow2 = (flags & GQ_SCALE_POW2) != 0;
