@@ -113,6 +113,7 @@ struct Smem {
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "fits one SM's shared memory");
 
 struct Params {
   const int32_t* offs;
@@ -312,10 +313,11 @@ __device__ __forceinline__ void fold_a(Unit& U, int ca, int cb, uint32_t tile, i
 // among the four lanes of a column leaves each lane 16 consecutive bytes of
 // a row of A^T (rows 16 q .. 16 q + 15 of the band), stored with one 16-byte
 // store.  Chunks outside [ca, cb) are computed from the window's other
-// columns and not stored.
+// columns and not stored.  The window's ring slot (`empty`) is released as
+// soon as the casts are in registers.
 __device__ __forceinline__ void quant_b(int32_t n0, int32_t xw, int ca, int cb,
-                                        const float* scale, uint32_t tile, const Params& p,
-                                        int lane) {
+                                        const float* scale, uint32_t tile, uint64_t* empty,
+                                        const Params& p, int lane) {
   const int q = lane & 3;
   const int mcol = lane >> 2;  // column within an 8-column chunk
   // this lane's stores: bytes n0 + 16 q .. + 15 of A^T rows
@@ -348,6 +350,10 @@ __device__ __forceinline__ void quant_b(int32_t n0, int32_t xw, int ca, int cb,
       w[cc][2 * qq + 1] = quant4(r[cc][2], r[cc][3], sv[4], sv[5], sv[6], sv[7]);
     }
   }
+  // the window is read: its slot goes back to the ring before the exchange
+  // and the stores, so that the loader can refill it sooner
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty);
   // lane q holds M[q][t] = w[.][t] for the four targets t; lane t needs
   // M[0..3][t].  Step 1 (partner q ^ 2) swaps the two words whose target
   // differs from q in bit 1, step 2 (partner q ^ 1) those differing in bit 0.
@@ -453,10 +459,8 @@ __device__ __forceinline__ bool pass_b(Smem& s, const UnitView& pv, uint32_t bas
                        : wait_load(s, ld, wait_ns, p.err);
       if (__any_sync(0xffffffffu, !ok)) return false;
       const uint32_t tile = pin(smem_addr(s.tile[ld % kStages]));
-      quant_b(pv.n0, pv.x0 + k * kTm, pv.lo - k * kTm, pv.hi - k * kTm, s.unit[ps].scale, tile, p,
-              lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.empty[ld % kStages]);
+      quant_b(pv.n0, pv.x0 + k * kTm, pv.lo - k * kTm, pv.hi - k * kTm, s.unit[ps].scale, tile,
+              &s.empty[ld % kStages], p, lane);
     }
   }
   j += static_cast<uint32_t>(pv.nst);
