@@ -18,10 +18,13 @@
 //   phase A -- a block folds a tile's column maxima, adds them to the
 //     strip's amax words in global memory (one atomicMax per column) and
 //     counts the tile on the strip's counter (a release reduction);
-//   phase B -- a block loads the tile again -- from L2: phase-A loads carry
-//     an L2 evict_last hint -- and, once the strip's counter shows all its
-//     tiles (an acquire load), reads the strip's amax words, computes its
-//     128 scales (448 / max(amax, 1e-12), IEEE division) and casts the tile.
+//   phase B -- in halves of a phase-A tile (kBSplit: so that a finished
+//     strip is re-read by more blocks at once and leaves L2 sooner), a
+//     block loads the rows again -- from L2: phase-A loads carry an L2
+//     evict_last hint -- and, once the strip's counter shows all its
+//     phase-A tiles (an acquire load), reads the strip's amax words,
+//     computes its 128 scales (448 / max(amax, 1e-12), IEEE division) and
+//     casts them.
 //
 // Each block runs two independent pipelines.  Both take work from global
 // counters in the same order -- slab by slab, strips in group order, tiles
@@ -30,16 +33,16 @@
 // never waits for other blocks, except that an item may not start before
 // the phase-B tiles up to `limit` tiles behind it have been taken -- the
 // phase-A data in flight, and so what L2 must hold until phase B re-reads
-// it, stays bounded (`limit`: the longest strip's tile count plus 2.5 slabs
-// of phase-B tiles, or 1.25 tiles per block if that is more); `limit`
-// exceeds the longest strip's tile count, so the
+// it, stays bounded (`limit`: the longest strip's phase-B tile count plus
+// 2.5 slabs of phase-B tiles, or 1.25 tiles per block if that is more);
+// `limit` exceeds the longest strip's phase-B tile count, so the
 // strips of those phase-B tiles precede the item and are all claimed, and
 // the wait always ends.  Phase B waits only for strips whose phase-A tiles
 // are all claimed.  Claims are made by running blocks, in order, and each
 // block works through its claims in order, so every wait ends whichever
 // blocks are resident (the launch needs no co-residency).
 //
-// Block roles (18 warps).  Phase one: a scheduler warp claims items (one
+// Block roles (16 warps).  Phase one: a scheduler warp claims items (one
 // ahead) and publishes a context per item in a ring of four -- few, so
 // that a claimed item is soon loaded and its strip soon complete; a
 // producer warp loads each item's stages -- 32 rows x 128 columns, 8 KB,
@@ -90,6 +93,7 @@ constexpr int kScale0 = kProdA + 4;             // 12 .. 15
 constexpr int kThreads = (kScale0 + kHelpers) * 32;
 constexpr int kRowBytes = kW * 2;
 constexpr int kStageBytes = kRows * kRowBytes;
+constexpr int kBSplit = 2;  // phase-B tiles per phase-A tile (when they stay >= kResRows rows)
 constexpr int kLeadQuarters = 10;  // phase-A lead: the longest strip + 2.5 slabs of phase-B tiles
 static_assert(kW == 128, "lane maps assume 128-column slabs");
 static_assert(kResStages <= kStages, "a resident strip fits the ring");
@@ -171,6 +175,8 @@ struct Params {
   unsigned* err;
   int32_t M, K, G;
   int32_t tile_rows;   // rows per two-phase tile: kTileRows, or less for small problems
+  int32_t tile_rows_b; // rows per phase-B tile: tile_rows / b_split
+  int32_t b_split;     // phase-B tiles per phase-A tile (kBSplit, or 1)
   int32_t forced_lag;  // > 0: the phase-A lead in slabs of phase-B tiles
   uint64_t timeout_ns;
   uint64_t clear_words;  // 32-bit words from `strip` to the end of the workspace
@@ -232,9 +238,10 @@ __device__ __forceinline__ void build_plan(Smem& s, const Params& p, int lane) {
     if (g < p.G) {
       const int32_t rows = s.ends[g] - (g ? s.ends[g - 1] : 0);
       const int32_t nt = (rows + p.tile_rows - 1) / p.tile_rows;
+      const int32_t ntb = (rows + p.tile_rows_b - 1) / p.tile_rows_b;
       const bool resident = rows <= kResRows && !p.two_phase;
       items = resident ? (rows > 0 ? 1 : 0) : nt;
-      bt = resident ? 0 : nt;
+      bt = resident ? 0 : ntb;
     }
     int32_t xi = items, xb = bt;  // inclusive scans
 #pragma unroll
@@ -343,7 +350,8 @@ __device__ __forceinline__ void sched_a(Smem& s, const Params& p, int lane) {
     const int32_t k = static_cast<int32_t>(j) - s.ip[g];
     const bool resident = s.bp[g + 1] == s.bp[g];
     // the throttle: phase-B tiles before this item, less the limit, must be taken
-    const int64_t before = static_cast<int64_t>(d) * pl.tb + s.bp[g] + (resident ? 0 : k);
+    const int64_t before =
+        static_cast<int64_t>(d) * pl.tb + s.bp[g] + (resident ? 0 : static_cast<int64_t>(k) * p.b_split);
     const int64_t need = before - pl.limit;
     taken = max(taken, fresh);
     if (need > static_cast<int64_t>(taken)) {
@@ -643,8 +651,8 @@ __device__ __forceinline__ void consumer_b(Smem& s, const Params& p, int w, int 
 
 // ------------------------------------------------------------------ scale --
 // The strip's last phase-B read returns its amax words and counter to zero:
-// the counter ends at 2 * ntiles (every phase-A tile, then every phase-B
-// read).  A read's atomic is issued with it and its result examined one
+// the counter ends at the strip's phase-A tiles plus its phase-B tiles
+// (every phase-A tile, then every phase-B read).  A read's atomic is issued with it and its result examined one
 // phase-B context later, so that its round trip is off the path.
 struct StripRead {
   uint32_t* word = nullptr;
@@ -656,7 +664,7 @@ struct StripRead {
 __device__ __forceinline__ void finish_read(StripRead& r, int lane) {
   if (r.word == nullptr) return;
   const uint32_t old = __shfl_sync(0xffffffffu, r.old, 0);
-  if (old + 1u == 2u * r.target) {
+  if (old + 1u == r.target) {
     if (r.am != nullptr) *reinterpret_cast<uint4*>(r.am) = make_uint4(0, 0, 0, 0);
     if (lane == 0) *r.word = 0u;
   }
@@ -698,14 +706,16 @@ __device__ __forceinline__ void scale_warp(Smem& s, const Params& p, int i, int 
     const uint32_t j = h - d * static_cast<uint32_t>(pl.tb);
     const int g = find_group(s.bp, p.G, static_cast<int32_t>(j), lane);
     if (lane == 0)
-      fill_ctx(c, s, p.tile_rows, kTypeB, g, static_cast<int32_t>(d), static_cast<int32_t>(j) - s.bp[g],
+      fill_ctx(c, s, p.tile_rows_b, kTypeB, g, static_cast<int32_t>(d), static_cast<int32_t>(j) - s.bp[g],
                0);
     __syncwarp();
     // the tile is published (and loaded) only once its strip is complete:
     // loaded earlier, it could come from HBM ahead of phase A, and it would
     // hold stage buffers while it waits
     uint32_t* word = p.strip + static_cast<size_t>(g) * pl.nsl + d;
-    const uint32_t target = static_cast<uint32_t>(c.ntiles);
+    const int32_t strip_rows = s.ends[g] - (g ? s.ends[g - 1] : 0);
+    const uint32_t target = static_cast<uint32_t>((strip_rows + p.tile_rows - 1) / p.tile_rows);
+    const uint32_t reads = static_cast<uint32_t>(c.ntiles);  // phase-B tiles of the strip
     const uint64_t t0 = global_timer_ns();
     for (;;) {
       const uint32_t v = ld_acquire_u32(word);
@@ -735,7 +745,7 @@ __device__ __forceinline__ void scale_warp(Smem& s, const Params& p, int i, int 
     finish_read(pend, lane);
     pend.word = word;
     pend.am = col < p.K ? am : nullptr;
-    pend.target = target;
+    pend.target = target + reads;  // the counter's final value
     pend.old = old;
     __syncwarp();
     if (lane == 0) mbar_arrive(&P.freed[ci]);
@@ -865,6 +875,8 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
       p.tile_rows = rows;
       break;
     }
+  p.b_split = p.tile_rows % kBSplit == 0 && p.tile_rows / kBSplit >= kResRows ? kBSplit : 1;
+  p.tile_rows_b = p.tile_rows / p.b_split;
   p.forced_lag = dbg.lag[GQ_KIND_COLWISE];
   p.timeout_ns = dbg.timeout_ns;
   p.clear_words = (L.total - L.counters) / 4;
