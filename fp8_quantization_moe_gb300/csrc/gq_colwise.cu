@@ -34,8 +34,8 @@
 // the phase-B tiles up to `limit` tiles behind it have been taken -- the
 // phase-A data in flight, and so what L2 must hold until phase B re-reads
 // it, stays bounded (`limit`: the longest strip's phase-B tile count plus
-// 2.5 slabs of phase-B tiles, or 1.25 tiles per block if that is more);
-// `limit` exceeds the longest strip's phase-B tile count, so the
+// 2.5 slabs of phase-B tiles, or 1.25 phase-A tiles per block if that is
+// more); `limit` exceeds the longest strip's phase-B tile count, so the
 // strips of those phase-B tiles precede the item and are all claimed, and
 // the wait always ends.  Phase B waits only for strips whose phase-A tiles
 // are all claimed.  Claims are made by running blocks, in order, and each
@@ -268,12 +268,13 @@ __device__ __forceinline__ void build_plan(Smem& s, const Params& p, int lane) {
     s.bp[p.G] = cb;
     const int32_t nsl = (p.K + kW - 1) / kW;
     // the lead: kLeadQuarters / 4 slabs of phase-B tiles, but never less
-    // than about one tile per block in flight, which phase one needs to keep
-    // every block busy (a slab of few tiles -- few rows, or uniform groups --
+    // than about one phase-A tile per block in flight, which phase one needs
+    // to keep every block busy (a slab of few tiles -- few rows, or uniform groups --
     // would otherwise starve it)
     const int64_t quarters = p.forced_lag > 0 ? 4 * static_cast<int64_t>(p.forced_lag) : kLeadQuarters;
     int64_t lead = quarters * cb / 4;
-    if (p.forced_lag <= 0) lead = max(lead, (5 * static_cast<int64_t>(gridDim.x)) / 4);
+    if (p.forced_lag <= 0)
+      lead = max(lead, (5 * static_cast<int64_t>(gridDim.x) * p.b_split) / 4);
     int64_t limit = static_cast<int64_t>(maxnt) + lead;
     if (limit > (int64_t(1) << 30)) limit = int64_t(1) << 30;
     s.plan.nsl = nsl;
