@@ -259,6 +259,24 @@ def test_colwise_resident_and_two_phase_strips(gq, widths, K):
     check_colwise(gq, synth.Case("strips_pow2", "colwise", base.x, offs, 0), pow2=True)
 
 
+@pytest.mark.parametrize("widths", [
+    # 11271 x 4096: 512-row phase-A tiles, read again as 256-row phase-B tiles
+    (511, 512, 513, 1023, 1024, 1025, 255, 256, 257, 0, 1, 3000, 2889),
+    # 17005 x 4096: 768-row phase-A tiles, read again as 384-row phase-B tiles
+    (383, 384, 385, 767, 768, 769, 1151, 1152, 1153, 1536, 1537, 0, 2000, 4000, 1015),
+])
+def test_colwise_split_phase_b_tiles(gq, widths):
+    """Sizes at which a 152-SM GB300 cuts long strips into 512- or 768-row
+    tiles, whose second read comes in halves: strips just inside and past a
+    half tile, a tile and one and a half tiles, empty, one-row and resident
+    strips mixed in one call, every column against the oracle."""
+    K = 4096
+    offs = np.cumsum(widths).astype(np.int32)
+    M = int(offs[-1]) + 5  # uncovered tail rows keep the sentinel
+    base = synth.random_case("colwise", M, K, 1, seed=400 + len(widths), scale_mix=True)
+    check_colwise(gq, synth.Case("split_" + str(M), "colwise", base.x, offs, 0))
+
+
 def test_short_super_tiles_many_tickets(gq):
     """Many short pieces of work: 512 column slabs of five short strips
     (colwise), or 1024 row bands of short groups (rowwise_t), so that every
