@@ -48,7 +48,7 @@
 // producer warp loads each item's stages -- 32 rows x 128 columns, 8 KB,
 // one TMA box -- into a ring of stage buffers; four consumer warps fold
 // (and for resident strips cast) them.  Phase B: a scheduler warp claims
-// tiles (two ahead) for a ring of eight contexts; four scale warps, context
+// tiles (two ahead) for a ring of four contexts; four scale warps, context
 // i to warp i % 4, decode the tile into its context (the producer warp
 // then loads it), wait for the strip and turn its amax words into the
 // scales; four consumer warps cast.  Stage v of a pipeline's stream goes to
@@ -77,7 +77,7 @@ constexpr int kTileRows = kTileStages * kRows;  // rows per two-phase tile (at m
 constexpr int kResStages = 8;                   // a strip of up to this many stages is resident
 constexpr int kResRows = kResStages * kRows;
 constexpr int kStages = 12;                     // stage ring of each pipeline
-constexpr int kCtx = 8;                         // contexts of the phase-B pipeline
+constexpr int kCtx = 4;                         // contexts of the phase-B pipeline
 constexpr int kCtxA = 4;                        // contexts of the phase-one pipeline
 constexpr int kAhead = 2;                       // phase-B claims made before they are needed
 constexpr int kCons = 4;                        // consumer warps of each pipeline
