@@ -24,10 +24,11 @@
 //     both operands MN-major: the token index is the contraction index and
 //     the operands are contiguous along n and k) and commits each stage back
 //     to the producer and each finished accumulator to the epilogue;
-//   warps 2-5: each reads its 32 TMEM lanes (rows n) with tcgen05.ld, 64
-//     columns at a time, scales (the scales of a tile are loaded two tiles
-//     ahead), rounds to bf16, stages the 32 rows' 128-byte runs in shared
-//     memory and stores them as whole lines.
+//   warps 2-9: two per TMEM lane quarter (32 rows n), each taking half of
+//     the tile's columns; each reads its lanes with tcgen05.ld, 32 columns
+//     at a time, scales (the scales of a tile are loaded two tiles ahead),
+//     rounds to bf16, stages the 32 rows' 64-byte runs in shared memory and
+//     stores them eight rows per instruction.
 // A group with no tokens gets zeros from the epilogue without any MMA.
 // Every wait is bounded; on expiry the error word is set, the warp leaves
 // its loop (as a whole: the lanes agree through __all_sync), the others
@@ -56,10 +57,11 @@ constexpr int kAOff = 2 * kBHalfBytes;
 static_assert(kABytes == kBHalfBytes, "three operand blocks of 16 KB, back to back");
 constexpr int kAccCols = kBN;              // fp32 TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;                // two per TMEM lane quarter
+constexpr int kEpiCols = kBN / 2;           // accumulator columns per epilogue warp
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr int kChunk = 64;                  // accumulator columns per epilogue step
-constexpr int kRowPitch = kChunk * 2 + 16;  // staged bf16 row: 128 bytes + 16 of padding
+constexpr int kChunk = 32;                  // accumulator columns per epilogue step: 64-byte runs
+constexpr int kStageRow = kChunk * 2;       // staged bf16 row (no padding: XOR-swizzled parts)
 static_assert(kTmemCols == 512, "two accumulators fill the TMEM");
 static_assert(kBM == 128 && kHalfN == 128 && kBK % kSubK == 0, "MMA shape");
 
@@ -72,11 +74,11 @@ struct Smem {
   uint64_t drain;             // the MMA warp's last commit
   uint32_t tmem_base;
   int32_t ends[kMaxGroups];
-  // per epilogue warp: 1/sx of the tile's columns, and 32 staged output rows
-  float rx[kEpiWarps][kBN];
-  alignas(16) uint8_t rows[kEpiWarps][32 * kRowPitch];
+  alignas(16) float rx[kEpiWarps][kEpiCols];  // per epilogue warp: 1/sx of its columns
+  alignas(16) uint8_t rows[kEpiWarps][32 * kStageRow];  // per epilogue warp: 32 staged row runs
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "fits one SM's shared memory");
 
 struct Params {
   const float* sa;       // (N, G)
@@ -180,7 +182,7 @@ struct TileId {
   int32_t g, n0, k0, t0, tg;  // group, first row, first column, first token, tokens
 };
 
-constexpr int kScaleLoads = kBN / 32;  // sx values per lane and tile
+constexpr int kScaleLoads = kEpiCols / 32;  // sx values per lane and tile
 
 __device__ __forceinline__ TileId tile_of(const Params& p, const int32_t* ends, int64_t i) {
   const int64_t per_group = static_cast<int64_t>(p.tiles_n) * p.tiles_k;
@@ -194,12 +196,12 @@ __device__ __forceinline__ TileId tile_of(const Params& p, const int32_t* ends, 
   return t;
 }
 
-// The raw scales epilogue lane `lane` of quarter q needs for tile i: sx of
-// columns k0 + lane + 32 m and sa of row n0 + 32 q + lane; 1.0 for columns
-// past K, rows past N and tiles past the last, so that every reciprocal
-// stays finite.
+// The raw scales epilogue lane `lane` of quarter q, column half hc, needs
+// for tile i: sx of columns k0 + kEpiCols hc + lane + 32 m and sa of row
+// n0 + 32 q + lane; 1.0 for columns past K, rows past N and tiles past the
+// last, so that every reciprocal stays finite.
 __device__ __forceinline__ void load_scales(const Params& p, const int32_t* ends, int64_t i, int q,
-                                            int lane, float (&x)[kScaleLoads], float& a) {
+                                            int hc, int lane, float (&x)[kScaleLoads], float& a) {
   if (i >= p.tiles) {
 #pragma unroll
     for (int m = 0; m < kScaleLoads; ++m) x[m] = 1.0f;
@@ -210,7 +212,7 @@ __device__ __forceinline__ void load_scales(const Params& p, const int32_t* ends
   const float* sxg = p.sx + static_cast<int64_t>(t.g) * p.K;
 #pragma unroll
   for (int m = 0; m < kScaleLoads; ++m) {
-    const int32_t k = t.k0 + lane + 32 * m;
+    const int32_t k = t.k0 + kEpiCols * hc + lane + 32 * m;
     x[m] = k < p.K ? __ldg(sxg + k) : 1.0f;
   }
   const int32_t n = t.n0 + 32 * q + lane;
@@ -357,17 +359,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- epilogue --
-    // Lane l of epilogue warp q owns row n0 + 32 q + l of the tile.  Per
-    // step of 64 columns it reads its row's accumulators, scales them,
-    // packs bf16 and writes the 128-byte run into the warp's staging rows;
-    // the warp then stores the 32 runs as whole lines, four rows per
-    // instruction.
+    // Lane l of epilogue warp (q, hc) owns row n0 + 32 q + l of the tile and
+    // the columns [kEpiCols hc, kEpiCols (hc + 1)).  Per step of 32 columns
+    // it reads its row's accumulators, scales them, packs bf16 and writes
+    // the row's 64-byte run into the warp's staging rows; the warp then
+    // stores the 32 runs, eight rows per instruction.  (One lane per row,
+    // each writing its own row, runs at three quarters of the rate: every
+    // store instruction would touch 32 lines.)  The four 16-byte parts of a
+    // staged run are XOR-swizzled by (row / 2) % 4, so that both the
+    // row-wise writes and the part-wise reads are free of bank conflicts.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ew = warp - 2;
+    const int hc = ew / 4;   // column half
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     float* rx = s.rx[ew];
-    uint8_t* rows = s.rows[ew];
-    const uint32_t my_row = smem_addr(rows + lane * kRowPitch);
+    const uint32_t stage_rows = smem_addr(s.rows[ew]);
+    const uint32_t my_row = stage_rows + static_cast<uint32_t>(lane * kStageRow);
+    const uint32_t my_swz = static_cast<uint32_t>((lane >> 1) & 3);
+    // the store side: lane j takes part j % 4 of rows 8 it + j / 4
+    const int part = lane & 3;
     // The scales of a tile are loaded two tiles ahead: under the TMA traffic
     // their latency is several microseconds, which would otherwise stall
     // every tile's epilogue.
@@ -375,20 +385,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     float x0[kScaleLoads], x1[kScaleLoads], x2[kScaleLoads];
     float a0, a1, a2;
-    load_scales(p, s.ends, blockIdx.x, q, lane, x0, a0);
-    load_scales(p, s.ends, blockIdx.x + static_cast<int64_t>(gridDim.x), q, lane, x1, a1);
+    load_scales(p, s.ends, blockIdx.x, q, hc, lane, x0, a0);
+    load_scales(p, s.ends, blockIdx.x + static_cast<int64_t>(gridDim.x), q, hc, lane, x1, a1);
     for (int64_t i = blockIdx.x; ok && i < p.tiles; i += gridDim.x) {
-      load_scales(p, s.ends, i + 2 * static_cast<int64_t>(gridDim.x), q, lane, x2, a2);
+      load_scales(p, s.ends, i + 2 * static_cast<int64_t>(gridDim.x), q, hc, lane, x2, a2);
       const TileId t = tile_of(p, s.ends, i);
+      const int32_t k0 = t.k0 + kEpiCols * hc;
       const int32_t nbase = t.n0 + 32 * q;
       const bool empty_group = t.tg <= 0;
       __syncwarp();  // the previous tile's readers of rx are done
-      // 1/sx of the tile's columns (0 past K), 1/sa of this lane's row
+      // 1/sx of the warp's columns (0 past K), 1/sa of this lane's row
 #pragma unroll
       for (int m = 0; m < kScaleLoads; ++m)
-        rx[lane + 32 * m] = t.k0 + lane + 32 * m < p.K ? __frcp_rn(x0[m]) : 0.0f;
-      const int32_t n = nbase + lane;
-      const float ra = n < p.N ? __frcp_rn(a0) : 0.0f;
+        rx[lane + 32 * m] = k0 + lane + 32 * m < p.K ? __frcp_rn(x0[m]) : 0.0f;
+      const float ra = nbase + lane < p.N ? __frcp_rn(a0) : 0.0f;
 #pragma unroll
       for (int m = 0; m < kScaleLoads; ++m) {
         x0[m] = x1[m];
@@ -404,60 +414,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       __syncwarp();  // rx visible to the warp
-      // TMEM loads run one half-chunk (32 columns) ahead of the math:
-      // h0 / h1 hold columns [64 ch, 64 ch + 32) / [64 ch + 32, 64 ch + 64).
-      const uint32_t tacc = tmem + lane_base + static_cast<uint32_t>(b * kAccCols);
-      uint32_t h0[32], h1[32];
-      if (!empty_group) tmem_ld32(tacc, h0);
-#pragma unroll 1
-      for (int ch = 0; ch < kBN / kChunk; ++ch) {
-        const int32_t kc = t.k0 + ch * kChunk;
-        uint32_t w[32];
+      // TMEM loads run one step ahead of the math (h[0] / h[1] alternate)
+      const uint32_t tacc =
+          tmem + lane_base + static_cast<uint32_t>(b * kAccCols + kEpiCols * hc);
+      uint32_t h[2][32];
+      if (!empty_group) tmem_ld32(tacc, h[0]);
+      uint8_t* orow0 = reinterpret_cast<uint8_t*>(p.out) +
+                       ((static_cast<int64_t>(t.g) * p.N + nbase) * p.K + k0) * 2 + part * 16;
+#pragma unroll
+      for (int st = 0; st < kEpiCols / kChunk; ++st) {
+        uint32_t(&hc_)[32] = h[st & 1];
+        uint32_t w[16];
         if (!empty_group) {
-          const float* rxc = rx + ch * kChunk;
-          tmem_ld_wait(h0);
-          tmem_ld32(tacc + static_cast<uint32_t>(ch * kChunk + 32), h1);
+          tmem_ld_wait(hc_);
+          if (st + 1 < kEpiCols / kChunk)
+            tmem_ld32(tacc + static_cast<uint32_t>((st + 1) * kChunk), h[(st + 1) & 1]);
+          const float* rxc = rx + st * kChunk;
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const __nv_bfloat162 v = __floats2bfloat162_rn(
-                __uint_as_float(h0[2 * e]) * ra * rxc[2 * e],
-                __uint_as_float(h0[2 * e + 1]) * ra * rxc[2 * e + 1]);
+                __uint_as_float(hc_[2 * e]) * ra * rxc[2 * e],
+                __uint_as_float(hc_[2 * e + 1]) * ra * rxc[2 * e + 1]);
             w[e] = *reinterpret_cast<const uint32_t*>(&v);
-          }
-          tmem_ld_wait(h1);
-          if (ch + 1 < kBN / kChunk)
-            tmem_ld32(tacc + static_cast<uint32_t>((ch + 1) * kChunk), h0);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const __nv_bfloat162 v = __floats2bfloat162_rn(
-                __uint_as_float(h1[2 * e]) * ra * rxc[32 + 2 * e],
-                __uint_as_float(h1[2 * e + 1]) * ra * rxc[32 + 2 * e + 1]);
-            w[16 + e] = *reinterpret_cast<const uint32_t*>(&v);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = 0u;
+          for (int e = 0; e < 16; ++e) w[e] = 0u;
         }
-        if (kc >= p.K) continue;  // warp-uniform; a load still in flight is waited for below
+        const int32_t kc = k0 + st * kChunk;
+        if (kc >= p.K) continue;  // warp-uniform: the rest of the row is past K
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          sts128(my_row + c * 16, make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]));
+        for (int c = 0; c < 4; ++c)
+          sts128(my_row + ((static_cast<uint32_t>(c) ^ my_swz) << 4),
+                 make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]));
         __syncwarp();
-        // lane j: row 4 i + j / 8, 16-byte part j % 8
-        const int part = lane & 7;
-        const int32_t k = kc + part * 8;
+        // K % 16 == 0: an 8-column part is wholly inside or outside
+        const bool k_ok = kc + part * 8 < p.K;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int row = 4 * it + (lane >> 3);
-          const uint4 v = lds128_ordered(smem_addr(rows + row * kRowPitch + part * 16));
-          const int32_t nr = nbase + row;
-          if (nr < p.N && k < p.K)
-            *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(t.g) * p.N + nr) * p.K + k) = v;
+        for (int it = 0; it < 4; ++it) {
+          const int row = 8 * it + (lane >> 2);
+          const uint32_t src = stage_rows + static_cast<uint32_t>(row * kStageRow) +
+                               ((static_cast<uint32_t>(part) ^ ((row >> 1) & 3)) << 4);
+          const uint4 v = lds128_ordered(src);
+          if (nbase + row < p.N && k_ok)
+            *reinterpret_cast<uint4*>(orow0 + static_cast<int64_t>(row) * p.K * 2 + st * kChunk * 2) = v;
         }
         __syncwarp();  // staging rows free for the next step
       }
-      if (!empty_group) tmem_ld_wait(h0);  // no TMEM load outlives the tile
       if (!empty_group) {
+        tmem_ld_wait(h[(kEpiCols / kChunk - 1) & 1]);  // no TMEM load outlives the tile
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !(p.skip_arrival && blockIdx.x == 0 && tc == 0))

@@ -79,6 +79,25 @@ def test_grouped_wgrad(gq, T, N, K, offs):
         s0 = max(s0, e)
 
 
+def test_grouped_wgrad_output_16_byte_aligned(gq):
+    """An output that is 16- but not 32-byte aligned (the contract asks for
+    16) takes 16-byte stores; the bytes before it are left alone."""
+    T, N, K, offs = 520, 272, 400, [130, 260, 390, 520]
+    case = synth.wgrad_case(T, N, K, offs, seed=907)
+    G = len(offs)
+    dev = torch.device("cuda")
+    buf = torch.full((G * N * K + 8,), 3.0, dtype=torch.bfloat16, device=dev)
+    out = buf[8:].view(G, N, K)
+    assert out.data_ptr() % 32 == 16
+    gq.grouped_wgrad(torch.from_numpy(case.qa_t).to(dev), torch.from_numpy(case.sa).to(dev),
+                     torch.from_numpy(case.qx).to(dev), torch.from_numpy(case.sx).to(dev),
+                     torch.from_numpy(case.offs).to(dev), out=out)
+    gq.check_device_error()
+    assert (buf[:8].float() == 3.0).all()
+    want, absum = oracle.grouped_wgrad(case.qa_t, case.sa, case.qx, case.sx, case.offs)
+    check(out.float().cpu().numpy().astype(np.float64), want, absum, "16-byte aligned output")
+
+
 def test_grouped_wgrad_no_tokens(gq):
     case = synth.wgrad_case(0, 32, 48, [0, 0], seed=901)
     dev = torch.device("cuda")
