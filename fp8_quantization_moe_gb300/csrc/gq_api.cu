@@ -232,7 +232,7 @@ size_t gq_workspace_bytes(int kind, int64_t rows, int64_t cols,
   if (kind == GQ_KIND_ROWWISE_T) {
     const int64_t N = rows, Mg = cols;
     if (N == 0 || Mg == 0) return 0;
-    return rowwise::kWorkspaceBytes;
+    return rowwise::workspace_bytes(N, Mg, n_groups);
   }
   return 0;
 }

@@ -63,7 +63,11 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
 namespace rowwise {
 constexpr int kTn = 64;  // rows of A per window: one row band
 constexpr int kTm = 64;  // token columns per window
-constexpr size_t kWorkspaceBytes = 256;  // unit counter, finished-blocks counter, padded
+constexpr size_t kHeaderBytes = 256;  // unit counter, finished-blocks counter, padded
+constexpr int kSplitWords = 68;        // per split unit: kTn amax words, a counter, padding
+// Workspace of a call: the header, then kSplitWords words for every
+// (row band, group) unit that may be split (groups of 4090 tokens or more).
+size_t workspace_bytes(int64_t N, int64_t Mg, int64_t G);
 gq_status setup(DeviceInfo& info);
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
                  int32_t N, int32_t Mg, const int32_t* offs, int32_t G,

@@ -22,7 +22,21 @@
 // A unit of at most kFit windows (groups up to about 760 tokens) keeps them
 // in shared memory between its two passes, and A is read from HBM once; a
 // longer unit streams its windows twice through the ring, the second time
-// from L2 where it can.
+// from L2 where it can.  Where groups are far longer (calls whose groups
+// average kSplitAvg tokens or more take a build that can do this), a unit of
+// more than kSplitOver windows -- whose two reads, for every row band at
+// once, would pass more data than L2 keeps between them -- is cut into parts
+// of at most kFit windows, consecutive tickets that other blocks take: each
+// part stays resident, adds its row maxima to the unit's words in the
+// workspace with atomicMax and counts itself (release); the descriptor warp
+// of each part, one unit later, waits for the count (acquire), takes the
+// scales and lets the part's pass B start.  Tickets are then assigned
+// (block b takes b, b + grid, ...), not claimed, so that a unit's parts lie
+// in two consecutive rounds of the grid, and a block's stream visits A of its
+// next unit before B of the current one; so a pass B waits only for passes
+// A that no wait precedes -- provided every block of the grid is resident,
+// which the blocks establish first (a count of arrivals and one CAS that
+// settles the decision for all), falling back to unsplit units otherwise.
 //
 // A descriptor warp claims units and publishes each in a small ring of unit
 // descriptors -- at most `lag` units in flight, about kBudget windows' worth
@@ -67,16 +81,25 @@
 #include "gq_device.cuh"
 #include "gq_internal.h"
 
+#include <algorithm>
+
 namespace gq {
 namespace rowwise {
 
 constexpr int kStages = 24;  // ring of windows
 constexpr int kFit = 12;     // windows a unit may keep resident between passes
+// A unit of more windows is split into parts of at most kFit windows that
+// several blocks take: read twice through the ring, such units (a group of
+// thousands of tokens in every row band) would pass more than L2 holds
+// between their two reads.
+constexpr int kSplitOver = 64;
+constexpr int kSplitAvg = 2048;  // average group (tokens) from which a call may split units
 constexpr int kUnits = 8;    // unit descriptors (at most in flight)
 constexpr int kBudget = 40;  // ring loads the units in flight should come to, about
 constexpr int kConsumerWarps = 10;
 constexpr int kAhead = 2;  // units a block claims before it needs them
 constexpr int kIssue = 8;  // producer lanes issuing window loads side by side
+constexpr uint64_t kResidentWaitNs = 200000;  // for every block of the grid to arrive
 constexpr int kLoaderWarp = kConsumerWarps;
 constexpr int kDescWarp = kConsumerWarps + 1;
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
@@ -86,10 +109,14 @@ static_assert(kTm * 2 == 128 && kTn == 64, "128-byte swizzled rows, two 32-row h
 static_assert(2 * kFit <= kStages, "the ring holds two consecutive resident units");
 static_assert(kUnits >= 2, "pass B of a resident unit follows pass A of the next");
 static_assert(kIssue <= kStages && kIssue <= 32, "a batch of loads takes distinct slots");
+static_assert(kSplitWords >= kTn + 1 && kSplitWords % 4 == 0, "amax words, counter, 16-byte rows");
 
 struct Unit {
   int32_t n0;   // first row of the band; -1: no more units
   int32_t g;    // group
+  int32_t sidx;   // split unit: its row of the split words; -1: not split
+  int32_t parts;  // parts of the split unit
+  int32_t part;   // this part (0 writes the scales)
   int32_t x0;   // token column of window 0 (s_g rounded down to 8)
   int32_t lo;   // group columns relative to x0: [lo, hi)
   int32_t hi;
@@ -110,6 +137,12 @@ struct Smem {
   uint64_t u_amax[kUnits];   // pass A done and scales written
   uint64_t u_free[kUnits];   // every warp's B visits done (W arrivals)
   int32_t ends[kMaxGroups];
+  // tickets of groups before g (tb[G] = all); split units of groups before
+  // g (sb[G] = all); both for the call's decomposition
+  int32_t tb[kMaxGroups + 1];
+  int32_t sb[kMaxGroups + 1];
+  int32_t split_mode;  // some unit is split: tickets are assigned, not claimed
+  int32_t clear_all;   // the last block clears the split words (after an error)
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
@@ -117,7 +150,10 @@ static_assert(kSmemBytes <= 227 * 1024, "fits one SM's shared memory");
 
 struct Params {
   const int32_t* offs;
-  uint32_t* ticket;  // unit counter; ticket[1]: blocks finished
+  uint32_t* ticket;  // unit counter; [1] blocks finished; [2] blocks arrived; [3] split decision
+  uint32_t* split;   // per split unit: kTn amax words and a counter (kSplitWords)
+  int32_t max_split; // split units the workspace has room for
+  uint64_t split_words;  // 32-bit words of the split region
   uint8_t* out_t;
   float* scales;
   unsigned* err;
@@ -155,33 +191,217 @@ __device__ __forceinline__ bool load_pass(Smem& s, const CUtensorMap* amap, uint
   return true;
 }
 
-// Claims units (kAhead ahead), decodes them and publishes their
-// descriptors; empty groups get their scales here and no descriptor.  The
-// whole warp builds the group-end table first.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* ptr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(ptr), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Windows of the group columns [s0, e0) (window 0 at s0 rounded down to 8).
+__device__ __forceinline__ int32_t windows_of(int32_t s0, int32_t e0) {
+  return (e0 - (s0 & ~7) + kTm - 1) / kTm;
+}
+
+// Parts each unit of a group is cut into: a unit of more than kSplitOver
+// windows into parts of at most kFit, so that every part stays resident.
+__device__ __forceinline__ int32_t parts_of(int32_t s0, int32_t e0) {
+  const int32_t w = e0 > s0 ? windows_of(s0, e0) : 0;
+  return w > kSplitOver ? (w + kFit - 1) / kFit : 1;
+}
+
+// Largest g in [0, n) with bands * pre[g] <= u, for a nondecreasing pre
+// with pre[0] = 0; a whole warp searches 32 probes at a time.
+__device__ __forceinline__ int find_group(const int32_t* pre, int n, uint32_t bands, uint32_t u,
+                                          int lane) {
+  int lo = 0, span = n;
+  while (span > 1) {
+    const int step = (span + 31) >> 5;
+    const int idx = lo + lane * step;
+    const bool le = idx < lo + span &&
+                    static_cast<uint64_t>(pre[idx]) * bands <= static_cast<uint64_t>(u);
+    const unsigned m = __ballot_sync(0xffffffffu, le);  // a prefix of the lanes, lane 0 set
+    const int nlo = lo + (31 - __clz(m)) * step;
+    span = min(step, lo + span - nlo);
+    lo = nlo;
+  }
+  return lo;
+}
+
+// A split unit's part at the end of its pass A: its row maxima join the
+// unit's words in global memory and the part is counted (release: after
+// the maxima).
+__device__ __forceinline__ void merge_part(uint32_t* w, const uint32_t* amax, bool count, int lane) {
+#pragma unroll
+  for (int qq = 0; qq < kQ; ++qq) {
+    const uint32_t a = amax[lane + 32 * qq];
+    if (a) atomicMax(w + lane + 32 * qq, a);
+  }
+  __syncwarp();
+  if (lane == 0 && count) red_release_add(w + kTn, 1u);
+}
+
+// The scales of split unit v, once every part's maxima are in its words
+// (the counter shows all parts: acquire); the unit's pass B may then start.
+// Each part's read is counted too, and the last of them returns the words
+// and the counter to zero.
+__device__ __forceinline__ bool split_scales(Smem& s, const Params& p, uint32_t v, int lane) {
+  Unit& U = s.unit[v % kUnits];
+  uint32_t* w = p.split + static_cast<size_t>(U.sidx) * kSplitWords;
+  const uint32_t parts = static_cast<uint32_t>(U.parts);
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    const uint32_t c = ld_acquire_u32(w + kTn);
+    if (__all_sync(0xffffffffu, c >= parts)) break;
+    if (ld_volatile_u32(p.err) != 0u || global_timer_ns() - t0 > p.timeout_ns) {
+      if (lane == 0) atomicOr(p.err, kErrDepTimeout);
+      return false;
+    }
+    __nanosleep(64);
+  }
+#pragma unroll
+  for (int qq = 0; qq < kQ; ++qq) {
+    const int r = lane + 32 * qq;
+    const float sc = scale_from_amax_bits(ld_cg_u32(w + r), p.pow2);
+    U.scale[r] = sc;
+    if (U.part == 0 && U.n0 + r < p.N) p.scales[static_cast<size_t>(U.n0 + r) * p.G + U.g] = sc;
+  }
+  __syncwarp();
+  if (lane == 0 && !U.hold) mbar_arrive(&s.u_amax[v % kUnits]);
+  uint32_t old = 0;
+  if (lane == 0) old = atom_add_acq_rel_gpu(w + kTn, 1u);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old + 1u == 2u * parts) {
+#pragma unroll
+    for (int qq = 0; qq < kQ; ++qq) w[lane + 32 * qq] = 0u;
+    __syncwarp();
+    if (lane == 0) w[kTn] = 0u;
+  }
+  return true;
+}
+
+// Decodes units and publishes their descriptors; empty groups get their
+// scales here and no descriptor.  The whole warp builds the group-end table
+// and the call's decomposition first.  Without split units, units are
+// claimed from the counter, kAhead ahead; with them, block b takes tickets
+// b, b + grid, b + 2 grid, ... (the parts of a split unit are consecutive
+// tickets, so they lie in two consecutive rounds of the grid, and every
+// block's stream visits A of its next unit before B of the current one: a
+// part's pass B waits only for passes A that no wait precedes).  One unit
+// behind its publication, a split unit's scales are taken here.
+template <bool kSplit>
 __device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int lane) {
   build_ends(p.offs, 0, p.G, p.Mg, s.ends, lane);
   __syncwarp();
+  // parts per unit of each group; prefix sums of parts and of split groups
+  // (only if some group is split at all)
+  bool any_split = false;
+  if (kSplit)
+    for (int g = lane; g < p.G; g += 32)
+      any_split |= parts_of(g ? s.ends[g - 1] : 0, s.ends[g]) > 1;
+  if (!__any_sync(0xffffffffu, any_split)) {
+    if (lane == 0) s.split_mode = 0;
+    __syncwarp();
+  } else {
+    int32_t cp = 0, cs = 0, maxp = 1;
+    for (int base = 0; base < p.G; base += 32) {
+      const int g = base + lane;
+      int32_t np = 0, sp = 0;
+      if (g < p.G) {
+        np = parts_of(g ? s.ends[g - 1] : 0, s.ends[g]);
+        sp = np > 1 ? 1 : 0;
+      }
+      int32_t xp = np, xs = sp;  // inclusive scans
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t yp = __shfl_up_sync(0xffffffffu, xp, o);
+        const int32_t ys = __shfl_up_sync(0xffffffffu, xs, o);
+        if (lane >= o) {
+          xp += yp;
+          xs += ys;
+        }
+      }
+      if (g < p.G) {
+        s.tb[g] = cp + xp - np;
+        s.sb[g] = cs + xs - sp;
+      }
+      cp += __shfl_sync(0xffffffffu, xp, 31);
+      cs += __shfl_sync(0xffffffffu, xs, 31);
+      maxp = max(maxp, np);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
+    // split only where a unit's parts fit one round of the grid, the
+    // workspace has the words, and every block of the grid is resident (a
+    // part waits for passes A that other blocks run): each block counts
+    // its arrival, and the first to see all of them -- or the first to
+    // give up waiting -- settles the decision for all (one CAS)
+    bool split = cs > 0 && maxp <= static_cast<int32_t>(gridDim.x) &&
+                 static_cast<int64_t>(cs) * p.bands <= p.max_split;
+    if (split) {
+      uint32_t d = 0;
+      if (lane == 0) {
+        atomicAdd(p.ticket + 2, 1u);
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+          d = ld_acquire_u32(p.ticket + 3);
+          if (d != 0u) break;
+          if (ld_acquire_u32(p.ticket + 2) >= gridDim.x) {
+            atomicCAS(p.ticket + 3, 0u, 1u);
+          } else if (global_timer_ns() - t0 > kResidentWaitNs) {
+            atomicCAS(p.ticket + 3, 0u, 2u);
+          } else {
+            __nanosleep(128);
+          }
+        }
+      }
+      split = __shfl_sync(0xffffffffu, d, 0) == 1u;
+    }
+    if (lane == 0) {
+      s.tb[p.G] = cp;
+      s.sb[p.G] = cs;
+      s.split_mode = split ? 1 : 0;
+    }
+    __syncwarp();
+  }
+  const bool split_mode = kSplit && s.split_mode != 0;
+  const uint32_t total = split_mode ? p.bands * static_cast<uint32_t>(s.tb[p.G]) : p.units;
   const uint64_t wait_ns = 4 * p.timeout_ns;
   uint32_t useq = 0;  // units published
+  bool pend = false;  // unit useq - 1 is split: its scales are due
   // lane 0 claims units kAhead ahead, so that a claim's round trip to L2
   // overlaps the units before it
   uint32_t q[kAhead];
 #pragma unroll
-  for (int a = 0; a < kAhead; ++a) q[a] = lane == 0 ? claim_ticket(p.ticket) : 0u;
+  for (int a = 0; a < kAhead; ++a)
+    q[a] = split_mode ? blockIdx.x + a * gridDim.x : lane == 0 ? claim_ticket(p.ticket) : 0u;
   for (;;) {
-    const uint32_t u = __shfl_sync(0xffffffffu, q[0], 0);
+    const uint32_t u = split_mode ? q[0] : __shfl_sync(0xffffffffu, q[0], 0);
 #pragma unroll
     for (int a = 0; a + 1 < kAhead; ++a) q[a] = q[a + 1];
-    if (lane == 0 && u < p.units) q[kAhead - 1] = claim_ticket(p.ticket);
-    int32_t grp = 0, n0 = -1, s0 = 0, e0 = 0;
-    if (u < p.units) {  // else: publish the stop descriptor
-      // group-major: the bands of a group are claimed one after another, so
+    if (split_mode)
+      q[kAhead - 1] = q[kAhead - 2] + gridDim.x;
+    else if (lane == 0 && u < total)
+      q[kAhead - 1] = claim_ticket(p.ticket);
+    int32_t grp = 0, n0 = -1, x0 = 0, lo = 0, hi = 0, nst = 0, sidx = -1, np = 1, part = 0;
+    if (u < total) {  // else: publish the stop descriptor
+      // group-major: the bands of a group are taken one after another, so
       // the 64-byte runs that neighbouring bands write into each row of A^T
-      // reach L2 close together
-      grp = static_cast<int32_t>(u / static_cast<uint32_t>(p.bands));
-      n0 = static_cast<int32_t>(u % static_cast<uint32_t>(p.bands)) * kTn;
-      s0 = grp ? s.ends[grp - 1] : 0;
-      e0 = s.ends[grp];
+      // reach L2 close together; a split unit's parts are consecutive
+      uint32_t r = u;
+      if (split_mode) {
+        grp = find_group(s.tb, p.G, p.bands, u, lane);
+        np = s.tb[grp + 1] - s.tb[grp];
+        r = u - p.bands * static_cast<uint32_t>(s.tb[grp]);
+        n0 = static_cast<int32_t>(r / static_cast<uint32_t>(np)) * kTn;
+        part = static_cast<int32_t>(r % static_cast<uint32_t>(np));
+      } else {
+        grp = static_cast<int32_t>(u / p.bands);
+        n0 = static_cast<int32_t>(u % p.bands) * kTn;
+      }
+      const int32_t s0 = grp ? s.ends[grp - 1] : 0, e0 = s.ends[grp];
       if (e0 == s0) {  // empty group: amax 0 for every row
         const float e = scale_from_amax_bits(0u, p.pow2);
 #pragma unroll
@@ -191,9 +411,21 @@ __device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int la
         }
         continue;
       }
+      if (np > 1) {
+        const int32_t w = windows_of(s0, e0);
+        const int32_t wa = part * w / np, wb = (part + 1) * w / np;
+        x0 = (s0 & ~7) + wa * kTm;
+        lo = s0 - x0;  // below 0 past part 0
+        hi = min(e0, (s0 & ~7) + wb * kTm) - x0;
+        nst = wb - wa;
+        sidx = s.sb[grp] * static_cast<int32_t>(p.bands) + n0 / kTn;
+      } else {
+        x0 = s0 & ~7;
+        lo = s0 - x0;
+        hi = e0 - x0;
+        nst = (hi + kTm - 1) / kTm;
+      }
     }
-    const int32_t x0 = s0 & ~7;
-    const int nst = n0 >= 0 ? (e0 - x0 + kTm - 1) / kTm : 0;
     const int us = static_cast<int>(useq % kUnits);
     // at most p.lag units in flight: unit useq - lag must be finished (units
     // finish in stream order), which also frees this descriptor
@@ -208,9 +440,14 @@ __device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int la
     if (lane == 0) {
       U.n0 = n0;
       U.g = grp;
+      if (kSplit) {
+        U.sidx = sidx;
+        U.parts = np;
+        U.part = part;
+      }
       U.x0 = x0;
-      U.lo = s0 - x0;
-      U.hi = e0 - x0;
+      U.lo = lo;
+      U.hi = hi;
       U.nst = nst;
       U.resident = nst <= kFit ? 1 : 0;
       U.hold = p.skip_arrival && u == 0u;
@@ -219,6 +456,11 @@ __device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int la
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.u_full[us]);
     ++useq;
+    // the previous unit's scales, now that this unit's pass A may run
+    if (kSplit) {
+      if (pend && !split_scales(s, p, useq - 2, lane)) return;
+      pend = sidx >= 0;
+    }
     if (n0 < 0) return;
   }
 }
@@ -404,6 +646,7 @@ __device__ __forceinline__ bool wait_load(Smem& s, uint32_t ld, uint64_t wait_ns
 
 // Pass A of unit `cu` (its windows are ring loads cu.first ...): this warp's
 // visits, and from the warp finishing the last of them the unit's scales.
+template <bool kSplit>
 __device__ __forceinline__ bool pass_a(Smem& s, const UnitView& cu, bool hold, uint32_t& j,
                                        const Params& p, int w, int lane, uint64_t wait_ns) {
   unsigned* err = p.err;
@@ -430,6 +673,12 @@ __device__ __forceinline__ bool pass_a(Smem& s, const UnitView& cu, bool hold, u
   if (lane == 0) prev = atom_add_acq_rel_cta_shared(smem_addr(&U.a_done), mine);
   prev = __shfl_sync(0xffffffffu, prev, 0);
   if (prev + mine == static_cast<uint32_t>(cu.nst)) {
+    if (kSplit && U.sidx >= 0) {
+      // a part of a split unit: its maxima join the unit's words at once;
+      // the descriptor warp takes the scales once every part is in
+      merge_part(p.split + static_cast<size_t>(U.sidx) * kSplitWords, U.amax, !hold, lane);
+      return true;
+    }
 #pragma unroll
     for (int qq = 0; qq < kQ; ++qq) {
       const int r = lane + 32 * qq;
@@ -469,6 +718,7 @@ __device__ __forceinline__ bool pass_b(Smem& s, const UnitView& pv, uint32_t bas
   return true;
 }
 
+template <bool kSplit>
 __device__ __forceinline__ void consumer_warp(Smem& s, const Params& p, int w, int lane) {
   const uint64_t wait_ns = 4 * p.timeout_ns;
   uint32_t g = 0;  // ring loads of the stream so far (the producer's count)
@@ -497,7 +747,7 @@ __device__ __forceinline__ void consumer_warp(Smem& s, const Params& p, int w, i
     }
     if (cu.resident) {
       g += static_cast<uint32_t>(cu.nst);
-      if (!pass_a(s, cu, hold, j, p, w, lane, wait_ns)) return;
+      if (!pass_a<kSplit>(s, cu, hold, j, p, w, lane, wait_ns)) return;
       if (pending && !pass_b(s, pv, pv.first, j, p, w, lane, wait_ns)) return;
       pv = cu;
       pending = true;
@@ -505,7 +755,7 @@ __device__ __forceinline__ void consumer_warp(Smem& s, const Params& p, int w, i
       if (pending && !pass_b(s, pv, pv.first, j, p, w, lane, wait_ns)) return;
       pending = false;
       g += static_cast<uint32_t>(cu.nst);
-      if (!pass_a(s, cu, hold, j, p, w, lane, wait_ns)) return;
+      if (!pass_a<kSplit>(s, cu, hold, j, p, w, lane, wait_ns)) return;
       const uint32_t base = g;  // the windows come again
       g += static_cast<uint32_t>(cu.nst);
       if (!pass_b(s, cu, base, j, p, w, lane, wait_ns)) return;
@@ -513,6 +763,7 @@ __device__ __forceinline__ void consumer_warp(Smem& s, const Params& p, int w, i
   }
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     rowwise_kernel(const __grid_constant__ CUtensorMap amap, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -536,42 +787,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   if (warp == kDescWarp)
-    descriptor_warp(s, p, lane);
+    descriptor_warp<kSplit>(s, p, lane);
   else if (warp == kLoaderWarp)
     loader_warp(s, &amap, p, lane);
   else
-    consumer_warp(s, p, warp, lane);
+    consumer_warp<kSplit>(s, p, warp, lane);
 
   // The last block to finish returns the counters to zero, so that the next
-  // call on this workspace may skip its clear (GQ_WORKSPACE_ZEROED).  Every
-  // block gets here, also after a bounded wait expired, and has made its
-  // last claim before its arrival is counted.
+  // call on this workspace may skip its clear (GQ_WORKSPACE_ZEROED); the
+  // split words return to zero with their last read.  Every block gets
+  // here, also after a bounded wait expired, and has made its last claim
+  // before its arrival is counted.
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
+    int32_t clear = 0;
     if (atomicAdd(p.ticket + 1, 1u) == gridDim.x - 1) {
       atomicExch(p.ticket, 0u);
       atomicExch(p.ticket + 1, 0u);
+      if (kSplit) {
+        // after an expired wait, split words may be left behind: clear them
+        clear = ld_volatile_u32(p.err) != 0u ? 1 : 0;
+        atomicExch(p.ticket + 2, 0u);
+        atomicExch(p.ticket + 3, 0u);
+      }
     }
+    if (kSplit) s.clear_all = clear;
+  }
+  if (kSplit) {
+    __syncthreads();
+    if (s.clear_all)
+      for (uint64_t i = threadIdx.x; i < p.split_words; i += blockDim.x) p.split[i] = 0u;
   }
 }
 
 // ---------------------------------------------------------------- host --
 gq_status setup(DeviceInfo& info) {
   gq_status st = check_cuda(
-      cudaFuncSetAttribute(rowwise_kernel,
+      cudaFuncSetAttribute(rowwise_kernel<false>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemBytes)),
       "rowwise_t: set shared memory size");
   if (st != GQ_OK) return st;
+  st = check_cuda(cudaFuncSetAttribute(rowwise_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes)),
+                  "rowwise_t: set shared memory size");
+  if (st != GQ_OK) return st;
   int occ = 0;
   st = check_cuda(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                      &occ, rowwise_kernel, kThreads, kSmemBytes),
+                      &occ, rowwise_kernel<true>, kThreads, kSmemBytes),
                   "rowwise_t: occupancy");
   if (st != GQ_OK) return st;
   if (occ < 1) return fail(GQ_ERR_UNSUPPORTED, "rowwise_t kernel does not fit an SM");
   info.rowwise_ctas_per_sm = occ;
   return GQ_OK;
+}
+
+size_t workspace_bytes(int64_t N, int64_t Mg, int64_t G) {
+  // a split unit's group has more than kSplitOver windows: at least
+  // kSplitOver * kTm - 6 tokens (window 0 starts up to 7 tokens early)
+  const int64_t bands = (N + kTn - 1) / kTn;
+  const int64_t max_groups = std::min<int64_t>(G, Mg / (kSplitOver * kTm - 6));
+  return kHeaderBytes + static_cast<size_t>(bands * max_groups) * kSplitWords * 4;
 }
 
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
@@ -588,13 +866,21 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
   Params p;
   const int64_t bands = (N + kTn - 1) / kTn;
   const int64_t units = bands * G;
+  // tickets: one per unit, or per part of a split unit; a part has at
+  // least kFit / 2 windows and a group of s tokens at most s / kTm + 2, so
+  // the groups give fewer than G + (Mg / kTm + 2 G) / (kFit / 2) parts
+  const int64_t tickets = bands * (G + (Mg / kTm + 2 * static_cast<int64_t>(G)) / (kFit / 2));
   const int64_t max_ctas = static_cast<int64_t>(info.sm_count) * info.rowwise_ctas_per_sm;
-  const int grid = static_cast<int>(units < max_ctas ? units : max_ctas);
-  // the unit counter ends below units + (kAhead + 1) * grid
-  if (units + (kAhead + 1) * static_cast<int64_t>(grid) >= (int64_t(1) << 32))
+  const int grid = static_cast<int>(tickets < max_ctas ? tickets : max_ctas);
+  // the counter ends below tickets + (kAhead + 1) * grid
+  if (tickets + (kAhead + 1) * static_cast<int64_t>(grid) >= (int64_t(1) << 32))
     return fail(GQ_ERR_UNSUPPORTED, "rowwise_t: (N / 64) x n_groups too large");
+  const size_t ws_bytes = workspace_bytes(N, Mg, G);
   p.offs = offs;
   p.ticket = static_cast<uint32_t*>(ws);  // first word of the header
+  p.split = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
+  p.split_words = (ws_bytes - kHeaderBytes) / 4;
+  p.max_split = static_cast<int32_t>(p.split_words / kSplitWords);
   p.out_t = static_cast<uint8_t*>(out_t);
   p.scales = scales;
   p.err = info.err_word;
@@ -618,10 +904,19 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
   p.pow2 = (flags & GQ_SCALE_POW2) != 0;
 
   if (!(flags & GQ_WORKSPACE_ZEROED)) {
-    st = check_cuda(cudaMemsetAsync(ws, 0, 8, stream), "rowwise_t: clear the counters");
+    st = check_cuda(cudaMemsetAsync(ws, 0, ws_bytes, stream), "rowwise_t: clear the workspace");
     if (st != GQ_OK) return st;
   }
-  rowwise_kernel<<<grid, kThreads, kSmemBytes, stream>>>(amap, p);
+  // A plain launch: units are claimed in order by running blocks and never
+  // wait for another block; split units are used only when the kernel has
+  // found every block of the grid resident (at most one per SM).  The build
+  // that can split is taken where groups average kSplitAvg tokens or more;
+  // the other reads every unit of more than kFit windows twice, which at
+  // shorter groups is faster.
+  if (Mg / G >= kSplitAvg)
+    rowwise_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(amap, p);
+  else
+    rowwise_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(amap, p);
   return check_cuda(cudaGetLastError(), "rowwise_t: launch");
 }
 

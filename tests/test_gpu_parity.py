@@ -240,6 +240,42 @@ def test_rowwise_resident_and_long_units(gq, widths, lead):
                                  "rowwise_t", base.x, offs, 0))
 
 
+@pytest.mark.parametrize("rows,widths,lead", [
+    (64, (16640,), 0),                       # one band: 22 parts of one unit
+    (208, (100, 900, 5000, 0, 4992), 4),     # short, long, split, empty, split
+    (144, (4091, 4089, 4097, 3, 9000), 5),   # around the split limit (64 windows)
+])
+def test_rowwise_split_units(gq, rows, widths, lead):
+    """Groups of more than 64 windows are cut into parts of at most 12
+    windows that other blocks take; the parts' row maxima meet in the
+    workspace before any part is cast.  Mixed with resident, long (13-64
+    windows, read twice) and empty groups."""
+    widths = list(widths)
+    Mg = lead + sum(widths)
+    Mg += (-Mg) % 8
+    offs = np.cumsum([lead + widths[0]] + widths[1:]).astype(np.int32)
+    base = synth.random_case("rowwise_t", rows, Mg, 1, seed=400 + rows, align=8,
+                             scale_mix=True)
+    check_rowwise(gq, synth.Case("split_" + "_".join(map(str, widths)), "rowwise_t",
+                                 base.x, offs, 0))
+
+
+def test_rowwise_split_timeout_is_reported_not_hung(gq):
+    """A part that never reports its maxima makes the other parts' scale
+    waits give up after the (shortened) limit: GQ_ERR_TIMEOUT, and the
+    workspace is left zeroed for the next call."""
+    r = synth.random_case("rowwise_t", 128, 8192, 1, seed=64)
+    try:
+        gq.debug_set(skip_arrival=True, wait_timeout_ns=5_000_000)
+        gq.rowwise_t(dev_bf16(r.x), dev_i32(r.offs))
+        with pytest.raises(gq.GQError) as e:
+            gq.check_device_error()
+        assert e.value.status == 4
+    finally:
+        gq.debug_set(False, 0)
+    check_rowwise(gq, r)
+
+
 @pytest.mark.parametrize("widths,K", [
     ((255, 256, 257, 1, 16, 0, 300), 400),            # around the resident limit
     ((767, 768, 769, 1536, 1537, 40), 272),           # around the tile size
@@ -465,13 +501,17 @@ def test_mxfp8_dim0(gq, M, K, mode):
 
 
 def test_rowwise_workspace_left_zeroed(gq):
-    """Every rowwise_t launch returns its counters to zero, so calls given
-    GQ_WORKSPACE_ZEROED on one workspace (zero-filled once) stay exact --
-    across shapes and group counts, and after a call without the flag."""
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    """Every rowwise_t launch returns its counters and split words to zero,
+    so calls given GQ_WORKSPACE_ZEROED on one workspace (zero-filled once)
+    stay exact -- across shapes and group counts (split units included), and
+    after a call without the flag."""
     cases = [synth.random_case("rowwise_t", 144, 520, 6, seed=70, n_empty=1, scale_mix=True),
              synth.random_case("rowwise_t", 1040, 3000, 9, seed=71, n_empty=1, align=1, uncovered=3),
-             synth.random_case("rowwise_t", 64, 16, 1, seed=72)]
+             synth.random_case("rowwise_t", 64, 16, 1, seed=72),
+             synth.random_case("rowwise_t", 192, 12000, 2, seed=73, scale_mix=True)]
+    nws = max(gq.workspace_bytes(gq.GQ_KIND_ROWWISE_T, c.x.shape[0], c.x.shape[1], len(c.offs))
+              for c in cases)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
     for rep in range(2):
         for c in cases:
             a, o = dev_bf16(c.x), dev_i32(c.offs)
@@ -480,10 +520,10 @@ def test_rowwise_workspace_left_zeroed(gq):
             st = gq.lib().gq_fp8_rowwise_t_ex(
                 a.data_ptr(), c.x.shape[0], c.x.shape[1], o.data_ptr(), len(c.offs),
                 qt.data_ptr(), s.data_ptr(), gq.GQ_WORKSPACE_ZEROED if rep == 0 else 0,
-                ws.data_ptr(), 256, torch.cuda.current_stream().cuda_stream)
+                ws.data_ptr(), nws, torch.cuda.current_stream().cuda_stream)
             assert st == 0
             gq.check_device_error()
-            assert not ws[:8].any().item(), "counters not returned to zero"
+            assert not ws.any().item(), "counters or split words not returned to zero"
             rq, rs = oracle.rowwise_t(c.x, c.offs, out=np.full((c.x.shape[1], c.x.shape[0]), SENTINEL, np.uint8))
             assert_same(qt.cpu().numpy(), s.cpu().numpy(), rq, rs, c.name)
 

@@ -63,7 +63,11 @@ def test_workspace_bytes(gq):
     # amax words
     assert gq.workspace_bytes(0, 100, 144, 3) == 256 + 256 + 1792
     # rowwise_t: a unit counter and a finished-blocks counter, padded
-    assert gq.workspace_bytes(1, 8192, 16640, 64) == 256
+    # rowwise_t: 256 B header + 68 words per (band, group) unit that may be
+    # split (groups of 4090 tokens or more: at most 16640 // 4090 = 4)
+    assert gq.workspace_bytes(1, 8192, 16640, 64) == 256 + 128 * 4 * 68 * 4
+    assert gq.workspace_bytes(1, 8192, 16640, 2) == 256 + 128 * 2 * 68 * 4
+    assert gq.workspace_bytes(1, 64, 4089, 8) == 256
     assert gq.workspace_bytes(0, 0, 4096, 4) == 0
     assert gq.workspace_bytes(1, 16, 0, 4) == 0
     assert gq.workspace_bytes(0, 16, 16, 0) == 0
