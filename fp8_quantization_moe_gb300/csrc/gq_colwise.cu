@@ -43,7 +43,7 @@
 // blocks are resident (the launch needs no co-residency).
 //
 // Block roles (16 warps).  Phase one: a scheduler warp claims items (one
-// ahead) and publishes a context per item in a ring of four -- few, so
+// ahead) and publishes a context per item in a ring of two -- few, so
 // that a claimed item is soon loaded and its strip soon complete; a
 // producer warp loads each item's stages -- 32 rows x 128 columns, 8 KB,
 // one TMA box -- into a ring of stage buffers; four consumer warps fold
@@ -78,7 +78,7 @@ constexpr int kResStages = 8;                   // a strip of up to this many st
 constexpr int kResRows = kResStages * kRows;
 constexpr int kStages = 12;                     // stage ring of each pipeline
 constexpr int kCtx = 4;                         // contexts of the phase-B pipeline
-constexpr int kCtxA = 4;                        // contexts of the phase-one pipeline
+constexpr int kCtxA = 2;                        // contexts of the phase-one pipeline
 constexpr int kAhead = 2;                       // phase-B claims made before they are needed
 constexpr int kCons = 4;                        // consumer warps of each pipeline
 constexpr int kHelpers = 4;                     // phase-B context i: scale warp i % 4

@@ -5,7 +5,9 @@
 // table.  Each kernel describes its own execution model in its file:
 //   gq_colwise.cu  (group, slab) strips: resident strips in one pass, longer
 //                  ones in two phases through L2, tickets from a counter;
-//   gq_rowwise.cu  block-local (row band, group) units, one HBM read;
+//   gq_rowwise.cu  (row band, group) units held in shared memory between
+//                  their two passes, one HBM read; a unit far longer than
+//                  the ring is cut into parts that several blocks take;
 //   gq_mxfp8.cu    a plain coalesced stream;
 //   gq_wgrad.cu    a tcgen05 grouped GEMM.
 //
