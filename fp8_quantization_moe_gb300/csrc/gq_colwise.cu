@@ -42,17 +42,17 @@
 // block works through its claims in order, so every wait ends whichever
 // blocks are resident (the launch needs no co-residency).
 //
-// Block roles (16 warps).  Phase one: a scheduler warp claims items (one
+// Block roles (18 warps).  Phase one: a scheduler warp claims items (one
 // ahead) and publishes a context per item in a ring of two -- few, so
 // that a claimed item is soon loaded and its strip soon complete; a
 // producer warp loads each item's stages -- 32 rows x 128 columns, 8 KB,
-// one TMA box -- into a ring of stage buffers; four consumer warps fold
+// one TMA box -- into a ring of stage buffers; six consumer warps fold
 // (and for resident strips cast) them.  Phase B: a scheduler warp claims
-// tiles (two ahead) for a ring of four contexts; four scale warps, context
-// i to warp i % 4, decode the tile into its context (the producer warp
+// tiles (two ahead) for a ring of two contexts; two scale warps, context
+// i to warp i % 2, decode the tile into its context (the producer warp
 // then loads it), wait for the strip and turn its amax words into the
-// scales; four consumer warps cast.  Stage v of a pipeline's stream goes to
-// its consumer warp v % 4.  Lane l of a consumer warp owns the 16-byte
+// scales; six consumer warps cast.  Stage v of a pipeline's stream goes to
+// its consumer warp v % 6.  Lane l of a consumer warp owns the 16-byte
 // column chunk l % 16 (8 columns) of stage rows l / 16, l / 16 + 2, ...:
 // every shared-memory access reads whole 256-byte rows (no swizzle
 // needed), a warp store writes two 128-byte output rows.
@@ -77,19 +77,19 @@ constexpr int kTileRows = kTileStages * kRows;  // rows per two-phase tile (at m
 constexpr int kResStages = 8;                   // a strip of up to this many stages is resident
 constexpr int kResRows = kResStages * kRows;
 constexpr int kStages = 12;                     // stage ring of each pipeline
-constexpr int kCtx = 4;                         // contexts of the phase-B pipeline
+constexpr int kCtx = 2;                         // contexts of the phase-B pipeline
 constexpr int kCtxA = 2;                        // contexts of the phase-one pipeline
 constexpr int kAhead = 2;                       // phase-B claims made before they are needed
-constexpr int kCons = 4;                        // consumer warps of each pipeline
-constexpr int kHelpers = 4;                     // phase-B context i: scale warp i % 4
+constexpr int kCons = 6;                        // consumer warps of each pipeline
+constexpr int kHelpers = 2;                     // phase-B context i: scale warp i % 2
 // warps
-constexpr int kConsA0 = 0;                      // 0 .. 3
-constexpr int kConsB0 = kCons;                  // 4 .. 7
-constexpr int kProdA = 2 * kCons;               // 8
-constexpr int kProdB = kProdA + 1;              // 9
-constexpr int kSchedA = kProdA + 2;             // 10
-constexpr int kSchedB = kProdA + 3;             // 11
-constexpr int kScale0 = kProdA + 4;             // 12 .. 15
+constexpr int kConsA0 = 0;                      // 0 .. 5
+constexpr int kConsB0 = kCons;                  // 6 .. 11
+constexpr int kProdA = 2 * kCons;               // 12
+constexpr int kProdB = kProdA + 1;              // 13
+constexpr int kSchedA = kProdA + 2;             // 14
+constexpr int kSchedB = kProdA + 3;             // 15
+constexpr int kScale0 = kProdA + 4;             // 16, 17
 constexpr int kThreads = (kScale0 + kHelpers) * 32;
 constexpr int kRowBytes = kW * 2;
 constexpr int kStageBytes = kRows * kRowBytes;
@@ -99,6 +99,7 @@ static_assert(kW == 128, "lane maps assume 128-column slabs");
 static_assert(kResStages <= kStages, "a resident strip fits the ring");
 static_assert(kStages % kCons == 0 && kStages <= 32, "stage waits stay within one phase");
 static_assert(kCtx % kHelpers == 0, "a context always has the same scale warp");
+static_assert(kCtxA <= kCtx, "both pipelines' contexts live in Pipe::ctx[kCtx]");
 
 constexpr int32_t kTypeA = 0;     // phase A of a tile of a long strip
 constexpr int32_t kTypeB = 1;     // phase B of a tile of a long strip
@@ -653,8 +654,9 @@ __device__ __forceinline__ void consumer_b(Smem& s, const Params& p, int w, int 
 // ------------------------------------------------------------------ scale --
 // The strip's last phase-B read returns its amax words and counter to zero:
 // the counter ends at the strip's phase-A tiles plus its phase-B tiles
-// (every phase-A tile, then every phase-B read).  A read's atomic is issued with it and its result examined one
-// phase-B context later, so that its round trip is off the path.
+// (every phase-A tile, then every phase-B read).  A read's atomic is
+// issued with it and its result examined one phase-B context later, so that
+// its round trip is off the path.
 struct StripRead {
   uint32_t* word = nullptr;
   uint32_t* am = nullptr;  // this lane's four amax words (nullptr: outside K)
