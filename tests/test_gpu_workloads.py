@@ -95,6 +95,26 @@ def test_rowwise_large(gq, idx, n_groups):
     assert torch.equal(s, sc.t())
 
 
+@pytest.mark.parametrize("kind,idx,n_groups", [("colwise", 3, 16), ("rowwise_t", 5, 64),
+                                                ("rowwise_t", 5, 1)])
+def test_repeated_launches_identical(gq, kind, idx, n_groups):
+    """Twenty launches back to back on one workspace -- the benchmark's
+    pattern -- give the first launch's bytes every time, whatever the
+    blocks' interleaving (claimed tiles, strip waits, and at one group the
+    parts of split units merging their maxima across blocks)."""
+    case = synth.workload(idx, n_groups)
+    x, offs = dev_bf16(case.x), dev_i32(case.offs)
+    call = gq.colwise if kind == "colwise" else gq.rowwise_t
+    q0, s0 = call(x, offs)
+    q0 = q0.view(torch.uint8).clone()
+    s0 = s0.clone()
+    for _ in range(20):
+        q, s = call(x, offs)
+        assert torch.equal(q.view(torch.uint8), q0)
+        assert torch.equal(s, s0)
+    gq.check_device_error()
+
+
 def test_pow2_scales_full_size(gq):
     """The two benchmark workloads with power-of-two scales, in full."""
     case = synth.workload(3, 16)
