@@ -96,7 +96,7 @@ constexpr int kSplitOver = 64;
 constexpr int kSplitAvg = 2048;  // average group (tokens) from which a call may split units
 constexpr int kUnits = 8;    // unit descriptors (at most in flight)
 constexpr int kBudget = 40;  // ring loads the units in flight should come to, about
-constexpr int kConsumerWarps = 10;
+constexpr int kConsumerWarps = 14;
 constexpr int kAhead = 2;  // units a block claims before it needs them
 constexpr int kIssue = 8;  // producer lanes issuing window loads side by side
 constexpr uint64_t kResidentWaitNs = 200000;  // for every block of the grid to arrive
