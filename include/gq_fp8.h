@@ -83,9 +83,16 @@ typedef enum gq_status {
  *   kind GQ_KIND_ROWWISE_T: rows = N, cols = Mg.
  * Colwise: a work counter, a finished-blocks counter, one counter per
  * (group, 128-column slab) strip and the per-(group, column) running amax
- * words.  Rowwise_t: a work counter and a finished-blocks counter (256
- * bytes), since each (row band, group) pair is finished by one thread
- * block.  The call clears what it uses itself, so the contents on entry do
+ * words.  Rowwise_t: a 256-byte header (a work counter, a finished-blocks
+ * counter, and two words with which the blocks settle whether all of them
+ * are resident), then 68 words per (64-row band, group) unit that may be
+ * split across blocks -- a group of 4090 tokens or more, so at most
+ * min(n_groups, Mg / 4090) per band: calls whose groups average 2048
+ * tokens or more cut such units (more than 64 windows of 64 tokens) into
+ * parts that several blocks take, which join their row maxima there; a
+ * call does so only when it finds every one of its blocks resident (at
+ * most one per SM), and otherwise runs those units whole, as the shorter
+ * ones.  The call clears what it uses itself, so the contents on entry do
  * not matter (with GQ_WORKSPACE_ZEROED the call skips the clear; see
  * there).  Returns 0 when no workspace is needed (empty problems) and for
  * invalid arguments.
