@@ -380,10 +380,11 @@ def check_device_error(stream=None, device=None):
         _check(lib().gq_check_device_error(sh), "gq_check_device_error")
 
 
-def debug_set(skip_arrival: bool = False, wait_timeout_ns: int = 0):
-    """Test hook: see gq_debug_set in include/gq_fp8.h."""
-    _check(lib().gq_debug_set(int(bool(skip_arrival)), int(wait_timeout_ns)),
-           "gq_debug_set")
+def debug_set(skip_arrival: bool = False, wait_timeout_ns: int = 0, no_split: bool = False):
+    """Test hooks: see gq_debug_set in include/gq_fp8.h (skip_arrival is
+    flag bit 0, no_split bit 1)."""
+    flags = int(bool(skip_arrival)) | (2 if no_split else 0)
+    _check(lib().gq_debug_set(flags, int(wait_timeout_ns)), "gq_debug_set")
 
 
 def set_lag(kind: int, lag: int = 0):

@@ -463,10 +463,13 @@ gq_status gq_set_lag(int kind, int32_t lag) {
   return GQ_OK;
 }
 
-gq_status gq_debug_set(int skip_arrival, int64_t wait_timeout_ns) {
+gq_status gq_debug_set(int flags, int64_t wait_timeout_ns) {
   if (wait_timeout_ns < 0)
     return fail(GQ_ERR_INVALID_ARG, "gq_debug_set: negative timeout");
-  g_dbg.skip_arrival = skip_arrival != 0;
+  if (flags & ~3)
+    return fail(GQ_ERR_INVALID_ARG, "gq_debug_set: unknown flags 0x%x", flags & ~3);
+  g_dbg.skip_arrival = flags & 1;
+  g_dbg.no_split = (flags >> 1) & 1;
   g_dbg.timeout_ns = wait_timeout_ns == 0 ? 1000000000ull
                                           : static_cast<uint64_t>(wait_timeout_ns);
   return GQ_OK;

@@ -24,6 +24,7 @@ struct DeviceInfo {
 // Launch-time knobs (test hooks).
 struct DebugKnobs {
   int skip_arrival = 0;
+  int no_split = 0;  // rowwise_t: never split units across blocks
   uint64_t timeout_ns = 1000000000ull;
   int32_t lag[2] = {0, 0};  // per kind; 0 = automatic
 };

@@ -163,6 +163,7 @@ struct Params {
   int32_t lag;     // units in flight per block (2 .. kUnits)
   uint64_t timeout_ns;
   int32_t skip_arrival;
+  int32_t no_split;  // test hook: units are never split
   bool pow2;  // scales rounded down to powers of two
 };
 
@@ -338,7 +339,7 @@ __device__ __forceinline__ void descriptor_warp(Smem& s, const Params& p, int la
     // part waits for passes A that other blocks run): each block counts
     // its arrival, and the first to see all of them -- or the first to
     // give up waiting -- settles the decision for all (one CAS)
-    bool split = cs > 0 && maxp <= static_cast<int32_t>(gridDim.x) &&
+    bool split = !p.no_split && cs > 0 && maxp <= static_cast<int32_t>(gridDim.x) &&
                  static_cast<int64_t>(cs) * p.bands <= p.max_split;
     if (split) {
       uint32_t d = 0;
@@ -901,6 +902,7 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* a,
   }
   p.timeout_ns = dbg.timeout_ns;
   p.skip_arrival = dbg.skip_arrival;
+  p.no_split = dbg.no_split;
   p.pow2 = (flags & GQ_SCALE_POW2) != 0;
 
   if (!(flags & GQ_WORKSPACE_ZEROED)) {

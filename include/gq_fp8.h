@@ -318,18 +318,24 @@ const char* gq_last_error(void);
 int gq_version(void);
 
 /*
- * Test hook for the bounded waits.  wait_timeout_ns sets the limit after
- * which a waiting kernel gives up (0 restores the 1 s default).
- * skip_arrival != 0 makes the next launches omit completion signals --
- * colwise: the first phase-A tile of every two-phase strip of the first
- * column slab, whose waiters are other thread blocks; rowwise_t: the amax-complete signal of the
- * (first row band, first group) unit, whose waiters are the warps that
- * would cast it; grouped_wgrad: the release of thread block 0's first TMEM
- * accumulator, whose waiter is the block's MMA warp -- so that the waiters
- * must time out and report GQ_ERR_TIMEOUT.  Process-wide; not thread-safe
- * with concurrent calls.
+ * Test hooks.  wait_timeout_ns sets the limit after which a waiting kernel
+ * gives up (0 restores the 1 s default).  flags (other bits are
+ * GQ_ERR_INVALID_ARG):
+ *   bit 0  the next launches omit a completion signal, so that its waiters
+ *          must time out and report GQ_ERR_TIMEOUT -- colwise: the count of
+ *          the first phase-A tile of every two-phase strip of the first
+ *          column slab (waiters: other thread blocks); rowwise_t: the
+ *          amax-complete signal of the (first row band, first group) unit
+ *          (waiters: the warps that would cast it), or, in a call that
+ *          splits units, the count of the first split unit's first part
+ *          (waiters: the other parts); grouped_wgrad: the release of thread
+ *          block 0's first TMEM accumulator (waiter: the block's MMA warp);
+ *   bit 1  rowwise_t never splits units across blocks (results are the
+ *          same; the path a call takes when it does not find all of its
+ *          blocks resident).
+ * Process-wide; not thread-safe with concurrent calls.
  */
-gq_status gq_debug_set(int skip_arrival, int64_t wait_timeout_ns);
+gq_status gq_debug_set(int flags, int64_t wait_timeout_ns);
 
 /*
  * Tuning knob for the phase interleave of `kind`.  The colwise kernel

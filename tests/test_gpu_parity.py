@@ -260,6 +260,26 @@ def test_rowwise_split_units(gq, rows, widths, lead):
                                  base.x, offs, 0))
 
 
+@pytest.mark.parametrize("rows,widths,lead", [(64, (16640,), 0),
+                                               (208, (100, 900, 5000, 0, 4992), 4)])
+def test_rowwise_split_build_without_splitting(gq, rows, widths, lead):
+    """The build that can split units, told not to (the path it takes when
+    it does not find every block resident): those units run whole, read
+    twice, and give the same bytes."""
+    widths = list(widths)
+    Mg = lead + sum(widths)
+    Mg += (-Mg) % 8
+    offs = np.cumsum([lead + widths[0]] + widths[1:]).astype(np.int32)
+    base = synth.random_case("rowwise_t", rows, Mg, 1, seed=410 + rows, align=8,
+                             scale_mix=True)
+    try:
+        gq.debug_set(no_split=True)
+        check_rowwise(gq, synth.Case("nosplit_" + "_".join(map(str, widths)), "rowwise_t",
+                                     base.x, offs, 0))
+    finally:
+        gq.debug_set(False, 0)
+
+
 def test_rowwise_split_timeout_is_reported_not_hung(gq):
     """A part that never reports its maxima makes the other parts' scale
     waits give up after the (shortened) limit: GQ_ERR_TIMEOUT, and the

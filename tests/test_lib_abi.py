@@ -119,6 +119,8 @@ def test_rowwise_host_validation(gq, args, status):
 
 def test_debug_set_rejects_negative_timeout(gq):
     assert gq.lib().gq_debug_set(0, -1) == 1
+    assert gq.lib().gq_debug_set(4, 0) == 1   # unknown flag bit
+    assert gq.lib().gq_debug_set(3, 0) == 0
     assert gq.lib().gq_debug_set(0, 0) == 0
 
 
