@@ -9,7 +9,7 @@
 //
 // Work is cut along the groups.  A strip is (group g, column slab d): the
 // group's rows by kW = 128 columns; every scale of a strip depends on that
-// strip alone.  A strip of at most kResRows = 256 rows is "resident": one
+// strip alone.  A strip of at most kResRows = 320 rows is "resident": one
 // block loads it once, folds its column maxima, computes its scales and
 // casts it out of shared memory (one HBM read, no other block involved).  A
 // longer strip is cut into tiles of kTileRows = 768 rows (fewer for small
@@ -74,8 +74,9 @@ namespace colwise {
 constexpr int kRows = 32;                       // rows per stage (one TMA box)
 constexpr int kTileStages = 24;                 // stages per two-phase tile (at most)
 constexpr int kTileRows = kTileStages * kRows;  // rows per two-phase tile (at most)
-constexpr int kResStages = 8;                   // a strip of up to this many stages is resident
+constexpr int kResStages = 10;                  // a strip of up to this many stages is resident
 constexpr int kResRows = kResStages * kRows;
+constexpr int kTileStep = 8 * kRows;  // 256 rows: the phase-A tile ladder's step, the least tile
 constexpr int kStages = 12;                     // stage ring of each pipeline
 constexpr int kCtx = 2;                         // contexts of the phase-B pipeline
 constexpr int kCtxA = 2;                        // contexts of the phase-one pipeline
@@ -93,7 +94,7 @@ constexpr int kScale0 = kProdA + 4;             // 16, 17
 constexpr int kThreads = (kScale0 + kHelpers) * 32;
 constexpr int kRowBytes = kW * 2;
 constexpr int kStageBytes = kRows * kRowBytes;
-constexpr int kBSplit = 2;  // phase-B tiles per phase-A tile (when they stay >= kResRows rows)
+constexpr int kBSplit = 2;  // phase-B tiles per phase-A tile (when they stay >= kTileStep rows)
 constexpr int kLeadQuarters = 10;  // phase-A lead: the longest strip + 2.5 slabs of phase-B tiles
 static_assert(kW == 128, "lane maps assume 128-column slabs");
 static_assert(kResStages <= kStages, "a resident strip fits the ring");
@@ -369,7 +370,10 @@ __device__ __forceinline__ void sched_a(Smem& s, const Params& p, int lane) {
       }
     }
     if (lane == 0)
-      fill_ctx(c, s, p.tile_rows, resident ? kTypeR : kTypeA, g, static_cast<int32_t>(d), k,
+      // a resident strip is one item, of up to kResRows rows (more than the
+      // least tile)
+      fill_ctx(c, s, resident ? kResRows : p.tile_rows, resident ? kTypeR : kTypeA, g,
+               static_cast<int32_t>(d), k,
                p.skip_arrival && !resident && d == 0 && k == 0);
     sts128(smem_addr(&c.amax[4 * lane]), make_uint4(0, 0, 0, 0));
     __syncwarp();
@@ -843,9 +847,9 @@ gq_status setup(DeviceInfo& info) {
 gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
                  int32_t M, int32_t K, const int32_t* offs, int32_t uniform, int32_t G,
                  void* out, float* scales, uint32_t flags, void* ws, cudaStream_t stream) {
-  // items and tiles are counted in 32 bits: at most one item per kResRows
+  // items and tiles are counted in 32 bits: at most one item per kTileStep
   // rows or group, per slab
-  const int64_t items = ((K + kW - 1) / kW) * ((M + kResRows - 1) / kResRows + G);
+  const int64_t items = ((K + kW - 1) / kW) * ((M + kTileStep - 1) / kTileStep + G);
   if (items >= (int64_t(1) << 31))
     return fail(GQ_ERR_UNSUPPORTED, "colwise: (M / 256 + n_groups) x (K / 128) too large");
   CUtensorMap xmap;
@@ -872,13 +876,13 @@ gq_status launch(const DeviceInfo& info, const DebugKnobs& dbg, const void* x,
   p.G = G;
   // the largest tile that still gives every block about four tiles per phase
   const int64_t max_ctas = static_cast<int64_t>(info.sm_count) * info.colwise_ctas_per_sm;
-  p.tile_rows = kResRows;
-  for (int32_t rows = kTileRows; rows > kResRows; rows -= kResRows)
+  p.tile_rows = kTileStep;
+  for (int32_t rows = kTileRows; rows > kTileStep; rows -= kTileStep)
     if (((K + kW - 1) / kW) * static_cast<int64_t>(M) / rows >= 4 * max_ctas) {
       p.tile_rows = rows;
       break;
     }
-  p.b_split = p.tile_rows % kBSplit == 0 && p.tile_rows / kBSplit >= kResRows ? kBSplit : 1;
+  p.b_split = p.tile_rows % kBSplit == 0 && p.tile_rows / kBSplit >= kTileStep ? kBSplit : 1;
   p.tile_rows_b = p.tile_rows / p.b_split;
   p.forced_lag = dbg.lag[GQ_KIND_COLWISE];
   p.timeout_ns = dbg.timeout_ns;

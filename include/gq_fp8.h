@@ -173,7 +173,7 @@ gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,
  *   GQ_TWO_PHASE   (colwise and expert_dim1 only; GQ_ERR_INVALID_ARG for
  *                  rowwise_t) every (group, 128-column slab) strip goes
  *                  through the two-phase path -- amax tiles, then a second
- *                  read for the cast -- also strips of at most 256 rows,
+ *                  read for the cast -- also strips of at most 320 rows,
  *                  which are otherwise loaded once and cast out of shared
  *                  memory.  Results are identical; the option exists to
  *                  test and time the two-phase path on any shape.
@@ -339,7 +339,7 @@ gq_status gq_debug_set(int flags, int64_t wait_timeout_ns);
 
 /*
  * Tuning knob for the phase interleave of `kind`.  The colwise kernel
- * visits every tile of a group strip longer than 256 rows twice -- phase A
+ * visits every tile of a group strip longer than 320 rows twice -- phase A
  * (amax) and phase B (scale + cast) -- and gives phase A a lead of `lag`
  * column slabs (128 columns each): phase A of slab d + lag is scheduled
  * alongside phase B of slab d.  A longer lead keeps phase B from waiting on

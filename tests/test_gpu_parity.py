@@ -297,12 +297,12 @@ def test_rowwise_split_timeout_is_reported_not_hung(gq):
 
 
 @pytest.mark.parametrize("widths,K", [
-    ((255, 256, 257, 1, 16, 0, 300), 400),            # around the resident limit
+    ((319, 320, 321, 1, 16, 0, 300, 256), 400),       # around the resident limit
     ((767, 768, 769, 1536, 1537, 40), 272),           # around the tile size
     ((256, 3000, 128, 0, 2305, 255, 17, 768), 1040),  # resident and long strips alternate
 ])
 def test_colwise_resident_and_two_phase_strips(gq, widths, K):
-    """Group strips of at most 256 rows are folded and cast by one block out
+    """Group strips of at most 320 rows are folded and cast by one block out
     of shared memory; longer ones go through the two phases in 768-row
     tiles.  Groups just inside and past both sizes, empty and one-row
     groups, mixed in one call, over several column slabs (the last one
