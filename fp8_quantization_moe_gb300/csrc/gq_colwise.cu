@@ -42,18 +42,19 @@
 // block works through its claims in order, so every wait ends whichever
 // blocks are resident (the launch needs no co-residency).
 //
-// Block roles (18 warps).  Phase one: a scheduler warp claims items (one
+// Block roles (22 warps).  Phase one: a scheduler warp claims items (one
 // ahead) and publishes a context per item in a ring of two -- few, so
 // that a claimed item is soon loaded and its strip soon complete; a
 // producer warp loads each item's stages -- 32 rows x 128 columns, 8 KB,
-// one TMA box -- into a ring of stage buffers; six consumer warps fold
+// one TMA box -- into a ring of stage buffers; twelve consumer warps fold
 // (and for resident strips cast) them.  Phase B: a scheduler warp claims
 // tiles (two ahead) for a ring of two contexts; two scale warps, context
 // i to warp i % 2, decode the tile into its context (the producer warp
 // then loads it), wait for the strip and turn its amax words into the
-// scales; six consumer warps cast.  Stage v of a pipeline's stream goes to
-// its consumer warp v % 6.  Lane l of a consumer warp owns the 16-byte
-// column chunk l % 16 (8 columns) of stage rows l / 16, l / 16 + 2, ...:
+// scales; four consumer warps cast.  Stage v of a pipeline's stream goes to
+// its consumer warp v % 12 (phase one) or v % 4 (phase B).  Lane l of a
+// consumer warp owns the 16-byte column chunk l % 16 (8 columns) of stage
+// rows l / 16, l / 16 + 2, ...:
 // every shared-memory access reads whole 256-byte rows (no swizzle
 // needed), a warp store writes two 128-byte output rows.
 //   fold: |x| folded with max.xorsign.abs.bf16x2, one shuffle joins the two
@@ -81,16 +82,17 @@ constexpr int kStages = 12;                     // stage ring of each pipeline
 constexpr int kCtx = 2;                         // contexts of the phase-B pipeline
 constexpr int kCtxA = 2;                        // contexts of the phase-one pipeline
 constexpr int kAhead = 2;                       // phase-B claims made before they are needed
-constexpr int kCons = 6;                        // consumer warps of each pipeline
+constexpr int kConsA = 12;                      // consumer warps of the phase-one pipeline
+constexpr int kConsB = 4;                       // consumer warps of the phase-B pipeline
 constexpr int kHelpers = 2;                     // phase-B context i: scale warp i % 2
 // warps
-constexpr int kConsA0 = 0;                      // 0 .. 5
-constexpr int kConsB0 = kCons;                  // 6 .. 11
-constexpr int kProdA = 2 * kCons;               // 12
-constexpr int kProdB = kProdA + 1;              // 13
-constexpr int kSchedA = kProdA + 2;             // 14
-constexpr int kSchedB = kProdA + 3;             // 15
-constexpr int kScale0 = kProdA + 4;             // 16, 17
+constexpr int kConsA0 = 0;                      // 0 .. 11
+constexpr int kConsB0 = kConsA;                 // 12 .. 15
+constexpr int kProdA = kConsA + kConsB;         // 16
+constexpr int kProdB = kProdA + 1;              // 17
+constexpr int kSchedA = kProdA + 2;             // 18
+constexpr int kSchedB = kProdA + 3;             // 19
+constexpr int kScale0 = kProdA + 4;             // 20, 21
 constexpr int kThreads = (kScale0 + kHelpers) * 32;
 constexpr int kRowBytes = kW * 2;
 constexpr int kStageBytes = kRows * kRowBytes;
@@ -98,7 +100,8 @@ constexpr int kBSplit = 2;  // phase-B tiles per phase-A tile (when they stay >=
 constexpr int kLeadQuarters = 10;  // phase-A lead: the longest strip + 2.5 slabs of phase-B tiles
 static_assert(kW == 128, "lane maps assume 128-column slabs");
 static_assert(kResStages <= kStages, "a resident strip fits the ring");
-static_assert(kStages % kCons == 0 && kStages <= 32, "stage waits stay within one phase");
+static_assert(kStages % kConsA == 0 && kStages % kConsB == 0 && kStages <= 32,
+              "stage waits stay within one phase");
 static_assert(kCtx % kHelpers == 0, "a context always has the same scale warp");
 static_assert(kCtxA <= kCtx, "both pipelines' contexts live in Pipe::ctx[kCtx]");
 
@@ -538,7 +541,7 @@ __device__ __forceinline__ void cast_stage(const Ctx& c, int v, uint32_t tile, i
 // out of order, so the load kStages before L may not be consumed yet and
 // the full barrier would still show its round: its release comes first.
 // (Loads L - kStages and L - 2 kStages belong to the same consumer warp --
-// kStages is a multiple of kCons -- which released them in order, so the
+// kStages is a multiple of the consumer count -- which released them in order, so the
 // empty barrier is never two phases behind here.)
 __device__ __forceinline__ bool wait_stage(Pipe& P, uint32_t L, uint64_t wait_ns, unsigned* err) {
   const int st = static_cast<int>(L % kStages);
@@ -564,9 +567,9 @@ __device__ __forceinline__ void consumer_a(Smem& s, const Params& p, int w, int 
     const int32_t type = c.type;
     if (type == kTypeStop) return;
     const int nsub = c.nsub;
-    const int v0 = (w + kCons - static_cast<int>(g % kCons)) % kCons;
+    const int v0 = (w + kConsA - static_cast<int>(g % kConsA)) % kConsA;
     uint32_t mine = 0;
-    for (int v = v0; v < nsub; v += kCons) {
+    for (int v = v0; v < nsub; v += kConsA) {
       ok = wait_stage(P, g + v, wait_ns, p.err);
       if (__any_sync(0xffffffffu, !ok)) return;
       const uint32_t tile = pin(smem_addr(P.tile[(g + v) % kStages]));
@@ -609,7 +612,7 @@ __device__ __forceinline__ void consumer_a(Smem& s, const Params& p, int w, int 
       if (type == kTypeR) {
         ok = mbar_wait(&P.ready[ci], par, wait_ns, p.err);
         if (__any_sync(0xffffffffu, !ok)) return;
-        for (int v = v0; v < nsub; v += kCons) {
+        for (int v = v0; v < nsub; v += kConsA) {
           const uint32_t tile = pin(smem_addr(P.tile[(g + v) % kStages]));
           cast_stage(c, v, tile, min(kRows, c.rows - v * kRows), p, lane);
           __syncwarp();
@@ -636,11 +639,11 @@ __device__ __forceinline__ void consumer_b(Smem& s, const Params& p, int w, int 
     const Ctx& c = P.ctx[ci];
     if (c.type == kTypeStop) return;
     const int nsub = c.nsub;
-    const int v0 = (w + kCons - static_cast<int>(g % kCons)) % kCons;
+    const int v0 = (w + kConsB - static_cast<int>(g % kConsB)) % kConsB;
     if (v0 < nsub) {
       ok = mbar_wait(&P.ready[ci], par, wait_ns, p.err);
       if (__any_sync(0xffffffffu, !ok)) return;
-      for (int v = v0; v < nsub; v += kCons) {
+      for (int v = v0; v < nsub; v += kConsB) {
         ok = wait_stage(P, g + v, wait_ns, p.err);
         if (__any_sync(0xffffffffu, !ok)) return;
         const uint32_t tile = pin(smem_addr(P.tile[(g + v) % kStages]));
@@ -782,8 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     for (int i = 0; i < kCtx; ++i) {
-      mbar_init(&s.a.freed[i], kCons);
-      mbar_init(&s.b.freed[i], kCons + 1);  // + the context's scale warp
+      mbar_init(&s.a.freed[i], kConsA);
+      mbar_init(&s.b.freed[i], kConsB + 1);  // + the context's scale warp
     }
     fence_mbar_init();
   }
