@@ -256,8 +256,9 @@ def test_rowwise_split_units(gq, rows, widths, lead):
     offs = np.cumsum([lead + widths[0]] + widths[1:]).astype(np.int32)
     base = synth.random_case("rowwise_t", rows, Mg, 1, seed=400 + rows, align=8,
                              scale_mix=True)
-    check_rowwise(gq, synth.Case("split_" + "_".join(map(str, widths)), "rowwise_t",
-                                 base.x, offs, 0))
+    case = synth.Case("split_" + "_".join(map(str, widths)), "rowwise_t", base.x, offs, 0)
+    check_rowwise(gq, case)
+    check_rowwise(gq, case, pow2=True)  # the split units' scales, rounded down
 
 
 @pytest.mark.parametrize("rows,widths,lead", [(64, (16640,), 0),
