@@ -679,8 +679,11 @@ def run_only(args):
     import fp8_quantization_moe_gb300 as gq
     from fp8_quantization_moe_gb300 import synth
 
+    if args.rowwise_no_split:
+        gq.debug_set(no_split=True)
     if args.only == "colwise":
         M, K, G = COLWISE_SHAPE
+        G = args.only_groups or G
         case = synth.colwise_large(G, rows=M, cols=K)
         nbytes = colwise_bytes(M, K, G)
         x = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -691,7 +694,9 @@ def run_only(args):
         workload = f"colwise X {M}x{K} bf16, {G} groups"
     else:
         N, Mg, G = ROWWISE_SHAPE
-        case = synth.rowwise_outliers(G, N=N, Mg=Mg)
+        G = args.only_groups or G
+        case = (synth.rowwise_g16() if G == 16 and (N, Mg) == (8192, 16640)
+                else synth.rowwise_outliers(G, N=N, Mg=Mg))
         nbytes = rowwise_bytes(N, Mg, G)
         a = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).to(dev)
         o = torch.from_numpy(case.offs).to(dev)
@@ -990,6 +995,11 @@ def main(argv=None):
     ap.add_argument("--only", choices=["colwise", "rowwise_t"], default=None,
                     help="time one kernel alone on its benchmark workload, launched "
                          "back to back (for profiling)")
+    ap.add_argument("--only-groups", type=int, default=0,
+                    help="with --only: the workload's group count (default: the benchmark's)")
+    ap.add_argument("--rowwise-no-split", action="store_true",
+                    help="with --only rowwise_t: never split units across blocks "
+                         "(the gq_debug_set flag), to compare the two paths")
     ap.add_argument("--no-graph", action="store_true",
                     help="time stream launches only (default: the step's two calls "
                          "replayed from CUDA graphs, stream launches reported beside)")
