@@ -63,6 +63,10 @@
 //   cast: each lane takes its chunk's eight scales from the context,
 //     multiplies in IEEE fp32 (mul.rn.f32x2) and packs with
 //     cvt.rn.satfinite.e4m3x2.
+// While one warp builds the plan at the start, the producer warp prefetches
+// the block's share of the first column slab's rows into L2 (TMA prefetches:
+// no shared memory, nothing to wait for), so that the first items' loads,
+// which the plan and the first claims delay by microseconds, find L2.
 // The last phase-B read of a strip returns its amax words and counter to
 // zero, and the last block to finish returns the work counters to zero, so
 // a workspace is left ready for the next call.
@@ -97,6 +101,7 @@ constexpr int kThreads = (kScale0 + kHelpers) * 32;
 constexpr int kRowBytes = kW * 2;
 constexpr int kStageBytes = kRows * kRowBytes;
 constexpr int kBSplit = 2;  // phase-B tiles per phase-A tile (when they stay >= kTileStep rows)
+constexpr int kWarmSlabs = 1;  // column slabs prefetched into L2 at the start
 constexpr int kLeadQuarters = 10;  // phase-A lead: the longest strip + 2.5 slabs of phase-B tiles
 static_assert(kW == 128, "lane maps assume 128-column slabs");
 static_assert(kResStages <= kStages, "a resident strip fits the ring");
@@ -217,6 +222,17 @@ __device__ __forceinline__ uint4 ld_cg_v4(const uint32_t* p) {
                : "l"(p)
                : "memory");
   return v;
+}
+
+// 2-D tiled TMA prefetch of one box into L2 (no shared memory, nothing to
+// wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "l"(policy)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
@@ -791,7 +807,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == kSchedA) build_plan(s, p, lane);
-  if (warp == kProdA && lane == 0) prefetch_tensormap(&xmap);
+  if (warp == kProdA) {
+    if (lane == 0) prefetch_tensormap(&xmap);
+    // while the plan is built: this block's share of the first kWarmSlabs
+    // column slabs, the first items' rows, prefetched into L2
+    const int32_t per = (p.M + static_cast<int32_t>(gridDim.x) - 1) / static_cast<int32_t>(gridDim.x);
+    const int32_t r0 = static_cast<int32_t>(blockIdx.x) * per;
+    const int32_t r1 = min(r0 + per, p.M);
+    const uint64_t pol = policy_evict_last();
+    for (int d = 0; d < kWarmSlabs && d * kW < p.K; ++d)
+      for (int32_t r = r0 + lane * kRows; r < r1; r += 32 * kRows)
+        tma_prefetch_2d(&xmap, d * kW, r, pol);
+  }
   __syncthreads();
 
   if (warp < kConsB0)
