@@ -154,6 +154,35 @@ def rowwise_outliers(n_groups: int = 64, seed: int | None = None,
                 to_bf16_bits(a), offs, seed, {"outlier_cols": np.sort(cols)})
 
 
+def past_int32(kind: str, rows: int, cols: int, n_groups: int, seed: int,
+               period: int = 4096, uncovered: int = 32) -> Case:
+    """An input of more than 2^31 elements, cheap to draw at 4 GB: a seeded
+    N(0,1) block of ``period`` rows (colwise: rows of X, shape (rows, cols);
+    rowwise_t: token columns of A, shape (cols, rows)) repeated along the
+    grouped dimension, repetition j scaled by 2^(j mod 8) -- an add to the
+    bf16 exponent field of the block's normal values, so exact -- so that a
+    result read or written at the wrong repetition differs.  The last
+    ``uncovered`` rows (tokens) lie past the last group."""
+    assert kind in ("colwise", "rowwise_t") and rows % ALIGN == 0
+    rng = np.random.default_rng(seed)
+    base = to_bf16_bits(_normal(rng, (period, cols)))
+    expo = base & np.uint16(0x7F80)
+    normal = (expo >= 0x0080) & (expo <= 0x7B80)  # room for +7 below inf
+    x = np.empty((rows, cols) if kind == "colwise" else (cols, rows), np.uint16)
+    for j in range((rows + period - 1) // period):
+        r0 = j * period
+        n = min(period, rows - r0)
+        blk = base[:n].copy()
+        blk[normal[:n]] += np.uint16((j % 8) << 7)
+        if kind == "colwise":
+            x[r0:r0 + n] = blk
+        else:
+            x[:, r0:r0 + n] = blk.T
+    offs = random_partition(rng, rows - uncovered, n_groups)
+    return Case(f"{kind}_{x.shape[0]}x{x.shape[1]}_g{n_groups}_past_int32", kind,
+                x, offs, seed)
+
+
 def workload(idx: int, n_groups: int | None = None) -> Case:
     """The five workloads, numbered 1..5 in the order listed above."""
     if idx == 1:

@@ -8,6 +8,7 @@ ones run the oracle over the host's cores in independent column (colwise)
 or row (rowwise_t) slices.  On top, properties that hold at any size: every
 group column (or row) with amax >= 1e-12 holds a +-448 code, no NaN code
 appears, and rowwise_t(A) equals colwise(A^T) with transposed scales.
+Past the workloads: both calls on inputs of more than 2^31 elements.
 """
 import numpy as np
 import pytest
@@ -161,3 +162,31 @@ def test_mxfp8_full_size(gq, mode):
     rq, rs = oracle_parallel.mxfp8_dim0(case.x, 0 if mode == "floor" else 1)
     assert np.array_equal(s.cpu().numpy(), rs)
     assert np.array_equal(q.view(torch.uint8).cpu().numpy(), rq)
+
+
+@pytest.mark.parametrize("kind,rows,cols,n_groups", [
+    ("colwise", 2 ** 19 + 64, 4096, 16),    # X (524352, 4096)
+    ("rowwise_t", 262160, 8192, 64),         # A (8192, 262160); units split across blocks
+])
+def test_past_2_31_elements(gq, kind, rows, cols, n_groups):
+    """More than 2^31 elements: every output offset past 2^31 has to be
+    formed in 64 bits.  Compared with the oracle in full, the rows (tokens)
+    past the last group keeping the sentinel."""
+    case = synth.past_int32(kind, rows, cols, n_groups, seed=1800 + n_groups)
+    assert case.x.size > 2 ** 31
+    x = dev_bf16(case.x)
+    offs = dev_i32(case.offs)
+    if kind == "colwise":
+        out = torch.full(case.x.shape, SENTINEL, dtype=torch.uint8, device="cuda")
+        q, s = gq.colwise(x, offs, out=out.view(torch.float8_e4m3fn))
+        ref = oracle_parallel.colwise
+    else:
+        out = torch.full(case.x.shape[::-1], SENTINEL, dtype=torch.uint8, device="cuda")
+        q, s = gq.rowwise_t(x, offs, out=out.view(torch.float8_e4m3fn))
+        ref = oracle_parallel.rowwise_t
+    gq.check_device_error()
+    del x
+    got_q, got_s = q.view(torch.uint8).cpu().numpy(), s.cpu().numpy()
+    del q, out
+    rq, rs = ref(case.x, case.offs, out=np.full(got_q.shape, SENTINEL, np.uint8))
+    assert_same(got_q, got_s, rq, rs, case.name)
