@@ -75,6 +75,8 @@ class Oracle:
         lib.gqo_mxfp8_dim0.restype = ctypes.c_int
         lib.gqo_expert_dim1.argtypes = [p, i64, i64, i64, ctypes.c_int, p, p]
         lib.gqo_expert_dim1.restype = ctypes.c_int
+        lib.gqo_expert_rowwise.argtypes = [p, i64, i64, i64, ctypes.c_int, p, p]
+        lib.gqo_expert_rowwise.restype = ctypes.c_int
         lib.gqo_scale_pow2_array.argtypes = [p, i64, p]
         lib.gqo_grouped_wgrad.argtypes = [p, p, p, p, i64, i64, i64, p, i32, p, p]
         lib.gqo_scale_pow2_array.restype = None
@@ -186,6 +188,21 @@ class Oracle:
         return q, s
 
 
+    def expert_rowwise(self, w_bf16_bits, pow2=False):
+        """Stacked expert weights (E, N, K) scaled per (expert, row), the
+        amax over the row's K elements.  Returns (q uint8 (E, N, K), scales
+        float32 (E, N))."""
+        w = _c(w_bf16_bits, np.uint16)
+        assert w.ndim == 3
+        E, N, K = w.shape
+        q = np.zeros((E, N, K), np.uint8)
+        s = np.empty((E, N), np.float32)
+        rc = self.lib.gqo_expert_rowwise(w.ctypes.data, E, N, K, int(bool(pow2)),
+                                         q.ctypes.data, s.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle expert_rowwise: invalid arguments")
+        return q, s
+
     def mxfp8_dim0(self, x_bf16_bits, mode):
         """mxfp8 cast along dim0: blocks of 32 consecutive elements of a row
         share a power-of-two scale.  mode 0 = FLOOR, 1 = RCEIL.  Returns
@@ -269,6 +286,10 @@ def rowwise_t(a_bf16_bits, offs, out=None, pow2=False):
 
 def expert_dim1(w_bf16_bits, pow2=False):
     return get().expert_dim1(w_bf16_bits, pow2)
+
+
+def expert_rowwise(w_bf16_bits, pow2=False):
+    return get().expert_rowwise(w_bf16_bits, pow2)
 
 
 def mxfp8_dim0(x_bf16_bits, mode):

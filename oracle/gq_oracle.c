@@ -20,7 +20,7 @@
  *     scale per (row, group) -- and the result is wanted transposed, so the
  *     fp8 output is written as A^T.
  * Further sections below: stacked expert weights along dim1 (#2863's PR
- * stack), the mxfp8 cast along dim0 (#3114), and the grouped grad_weight
+ * stack) and per row (#2668's PR stack), the mxfp8 cast along dim0 (#3114), and the grouped grad_weight
  * product of the two quantized operands (#2668's MoE fp8 training test).
  *
  * Per group g with token range [s_g, e_g) and each column (colwise) or row
@@ -295,6 +295,34 @@ int gqo_expert_dim1(const uint16_t* w, int64_t E, int64_t K, int64_t N, int pow2
       scales[e * N + n] = s;
       for (k = 0; k < K; ++k)
         q[(e * K + k) * N + n] = gqo_quant(w[(e * K + k) * N + n], s);
+    }
+  return 0;
+}
+
+/*
+ * Stacked expert weights w: bf16 bits, (E, N, K) row-major, scaled per row:
+ * one scale for each expert e and row n, the amax taken over that row's K
+ * elements (the "fp8 rowwise kernels for expert weights" of the #2668
+ * page's PR stack, #2696); q has w's layout, scales are (E, N) row-major.
+ * Returns 0, or -1 on invalid arguments.
+ */
+int gqo_expert_rowwise(const uint16_t* w, int64_t E, int64_t N, int64_t K, int pow2,
+                       uint8_t* q, float* scales) {
+  int64_t e, n, k;
+  if (E < 1 || N < 0 || K < 0) return -1;
+  if ((E * N * K > 0) && (w == NULL || q == NULL)) return -1;
+  if (N > 0 && scales == NULL) return -1;
+  for (e = 0; e < E; ++e)
+    for (n = 0; n < N; ++n) {
+      const int64_t row = (e * N + n) * K;
+      float amax = 0.0f, s;
+      for (k = 0; k < K; ++k) {
+        float a = fabsf(gqo_bf16_to_float(w[row + k]));
+        if (a > amax) amax = a;
+      }
+      s = gqo_scale_opt(amax, pow2);
+      scales[e * N + n] = s;
+      for (k = 0; k < K; ++k) q[row + k] = gqo_quant(w[row + k], s);
     }
   return 0;
 }

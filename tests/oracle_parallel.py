@@ -81,6 +81,24 @@ def expert_dim1(w: np.ndarray, pow2: bool = False):
     return q, s
 
 
+def expert_rowwise(w: np.ndarray, pow2: bool = False):
+    """oracle.expert_rowwise on the whole of W (E, N, K), in slices of rows
+    (dim 1); returns (q (E, N, K), scales (E, N))."""
+    E, N, K = w.shape
+    q = np.zeros((E, N, K), np.uint8)
+    s = np.empty((E, N), np.float32)
+
+    def one(n0):
+        n1 = min(N, n0 + SLICE)
+        qs, ss = oracle.expert_rowwise(np.ascontiguousarray(w[:, n0:n1]), pow2=pow2)
+        q[:, n0:n1] = qs
+        s[:, n0:n1] = ss
+
+    with cf.ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, range(0, N, SLICE)))
+    return q, s
+
+
 def mxfp8_dim0(x: np.ndarray, mode: int):
     """oracle.mxfp8_dim0 on the whole of X (M, K), in row slices (every
     32-element row block is independent)."""

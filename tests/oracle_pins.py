@@ -365,6 +365,42 @@ def pin_expert_dim1(o):
             assert np.array_equal(qc, q.reshape(E * K, N)) and np.array_equal(sc, s)
 
 
+def pin_expert_rowwise(o):
+    """Stacked expert weights per row: a numpy / torch restatement of the
+    definition (per expert and row: amax over the row's K elements, fp32
+    scale, torch's RNE-saturating e4m3 cast of the fp32 product) on ragged
+    small shapes with per-row magnitudes over six decades, K = 0 and N = 0
+    included, plain and power-of-two scales; and the identity with rowwise_t
+    on each expert's (N, K) matrix as one group of K tokens, whose output is
+    the transpose."""
+    rng = np.random.default_rng(53)
+    for E, N, K in ((1, 5, 16), (3, 7, 40), (2, 4, 0), (2, 0, 8), (2, 9, 33)):
+        x = rng.standard_normal((E, N, K)).astype(np.float32)
+        x *= np.power(np.float32(10), rng.uniform(-3, 3, size=(E, N, 1))).astype(np.float32)
+        if N > 1 and K:
+            x[0, 1] = 0.0  # an all-zero row: scale 448 / 1e-12
+        w = synth.to_bf16_bits(x)
+        wf = ref_loop.bf16_bits_to_f32(w)
+        amax = np.abs(wf).max(axis=2) if K else np.zeros((E, N), np.float32)
+        se = (np.float32(448.0) / np.maximum(amax, np.float32(1e-12))).astype(np.float32)
+        for pow2 in (False, True):
+            q, s = o.expert_rowwise(w, pow2=pow2)
+            assert q.shape == (E, N, K) and s.shape == (E, N)
+            if pow2:  # a power of two at or below the plain scale, above half of it
+                mant, _ = np.frexp(s.astype(np.float64))
+                assert np.all(mant == 0.5) and np.all(s <= se) and np.all(se < 2 * s), (E, N, K)
+            else:
+                assert np.array_equal(s, se), (E, N, K)
+            if K and N:
+                v = (wf * s[:, :, None]).astype(np.float32)
+                assert np.array_equal(q, _torch_e4m3(np.clip(v, -448, 448))), (E, N, K, pow2)
+        if K and N:
+            q, s = o.expert_rowwise(w)
+            for e in range(E):
+                qt, st = o.rowwise_t(np.ascontiguousarray(w[e]), np.array([K], np.int32))
+                assert np.array_equal(qt.T, q[e]) and np.array_equal(st[:, 0], s[e])
+
+
 def _mx_input(rng, M, K):
     """Rows of blocks with magnitudes from 2^-140 to 2^120, zero blocks,
     bf16 subnormals, signed zeros and exact powers of two."""
@@ -480,6 +516,6 @@ ALL_PINS = [
     pin_scale_exact, pin_quant_single_rounding, pin_hand_examples,
     pin_paths_vs_library_loop, pin_out_of_contract_offsets,
     pin_transpose_identity, pin_max_code_invariant, pin_dequant_bound,
-    pin_scale_pow2, pin_pow2_paths, pin_expert_dim1, pin_mxfp8_dim0,
+    pin_scale_pow2, pin_pow2_paths, pin_expert_dim1, pin_expert_rowwise, pin_mxfp8_dim0,
     pin_wgrad_hand, pin_wgrad_vs_matmul,
 ]

@@ -52,6 +52,10 @@ MUTANTS = {
     "mx_zero_block": ("if (amax == 0.0f) return -127;", "if (amax == 0.0f) return 0;"),
     "expert_amax_ignores_expert": ("float a = fabsf(gqo_bf16_to_float(w[(e * K + k) * N + n]));",
                                    "float a = fabsf(gqo_bf16_to_float(w[k * N + n]));"),
+    "expert_rowwise_amax_of_first_row": ("float a = fabsf(gqo_bf16_to_float(w[row + k]));",
+                                         "float a = fabsf(gqo_bf16_to_float(w[e * N * K + k]));"),
+    "expert_rowwise_scale_of_previous_row": ("for (k = 0; k < K; ++k) q[row + k] = gqo_quant(w[row + k], s);",
+                                             "for (k = 0; k < K; ++k) q[row + k] = gqo_quant(w[row + k], n ? scales[e * N + n - 1] : s);"),
     "wgrad_drops_last_token": ("for (t = start[g]; t < end[g]; ++t)\n      for (n = 0; n < N; ++n) {",
                                "for (t = start[g]; t + 1 < end[g]; ++t)\n      for (n = 0; n < N; ++n) {"),
     "wgrad_operand_transposed": ("const double a = dec[qa_t[t * N + n]];",

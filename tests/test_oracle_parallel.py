@@ -35,6 +35,10 @@ def test_expert_and_mxfp8_slices_equal_whole():
     q1, s1 = oracle.expert_dim1(w)
     q2, s2 = oracle_parallel.expert_dim1(w)
     assert np.array_equal(q1, q2) and np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+    w = synth.to_bf16_bits(rng.standard_normal((3, 600, 40)).astype(np.float32))
+    q1, s1 = oracle.expert_rowwise(w)
+    q2, s2 = oracle_parallel.expert_rowwise(w)
+    assert np.array_equal(q1, q2) and np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
     x = synth.to_bf16_bits(rng.standard_normal((2100, 96)).astype(np.float32))
     for mode in (0, 1):
         q1, s1 = oracle.mxfp8_dim0(x, mode)
