@@ -613,7 +613,12 @@ def per_config_block(dev, steps: int = 20):
     med, mean = _time_calls(lambda: gq.expert_dim1(wd, out=qe, scales=se), steps)
     out[f"expert_dim1_{E}x{Ke}x{Ne}"] = rec(med, mean, 3 * E * Ke * Ne + 4 * E * Ne,
                                             l2="input larger than L2")
-    del wd, qe
+    # the same weights read as (E, N, K) and scaled per (expert, row)
+    sr = torch.empty((E, Ke), dtype=torch.float32, device=dev)
+    med, mean = _time_calls(lambda: gq.expert_rowwise(wd, out=qe, scales=sr), steps)
+    out[f"expert_rowwise_{E}x{Ke}x{Ne}"] = rec(med, mean, 3 * E * Ke * Ne + 4 * E * Ke,
+                                               l2="input larger than L2")
+    del wd, qe, sr
     torch.cuda.empty_cache()
     # the grouped grad_weight GEMM
     T, N, K, G = WGRAD_SHAPE

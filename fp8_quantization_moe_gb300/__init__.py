@@ -8,6 +8,8 @@ Two paths, both in hand-written sm_103a CUDA kernels behind the C ABI of
   output written transposed;
 * ``expert_dim1(w)``     -- stacked expert weights (E, K, N): one scale per
   (expert, column), reduced along dim1;
+* ``expert_rowwise(w)``  -- stacked expert weights (E, N, K): one scale per
+  (expert, row);
 * ``mxfp8_dim0(x, mode)`` -- mxfp8: 32-element row blocks with e8m0 scales
   (FLOOR or RCEIL);
 * ``grouped_wgrad(qa_t, sa, qx, sx, offs)`` -- the consumer of the two
@@ -21,7 +23,7 @@ supplies device memory and streams.  ``synth`` draws seeded inputs.
 """
 from ._binding import (GQ_KIND_COLWISE, GQ_KIND_ROWWISE_T, GQ_MAX_GROUPS,
                        GQ_SCALE_POW2, GQ_TWO_PHASE, GQ_WORKSPACE_ZEROED, GQError, check_device_error, colwise, colwise_host,
-                       colwise_noalloc, expert_dim1, mxfp8_dim0,
+                       colwise_noalloc, expert_dim1, expert_rowwise, mxfp8_dim0,
                        grouped_wgrad, debug_set, lib, library_path, rowwise_t,
                        rowwise_t_host, set_lag, status_string, version,
                        workspace_bytes)
@@ -31,7 +33,8 @@ __all__ = [
     "GQ_KIND_COLWISE", "GQ_KIND_ROWWISE_T", "GQ_MAX_GROUPS", "GQ_SCALE_POW2", "GQ_TWO_PHASE",
     "GQ_WORKSPACE_ZEROED", "GQError",
     "build", "check_device_error", "colwise", "colwise_host",
-    "colwise_noalloc", "debug_set", "expert_dim1", "grouped_wgrad", "mxfp8_dim0",
+    "colwise_noalloc", "debug_set", "expert_dim1", "expert_rowwise", "grouped_wgrad",
+    "mxfp8_dim0",
     "lib", "library_path", "rowwise_t", "rowwise_t_host", "set_lag",
     "status_string",
     "version", "workspace_bytes",

@@ -38,6 +38,7 @@ SIGNATURES = {
     "gq_fp8_colwise_noalloc": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P]),
     "gq_fp8_colwise_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
     "gq_fp8_expert_dim1": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
+    "gq_fp8_expert_rowwise": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, ctypes.c_uint32, _P]),
     "gq_mxfp8_dim0": (ctypes.c_int, [_P, _I64, _I64, _P, _P, ctypes.c_int, _P]),
     "gq_grouped_wgrad": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I32, _P, _P]),
     "gq_fp8_rowwise_t_ex": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, ctypes.c_uint32, _P, _SZ, _P]),
@@ -277,6 +278,32 @@ def expert_dim1(w: torch.Tensor, *, out=None, scales=None, stream=None, workspac
         st = lib().gq_fp8_expert_dim1(_ptr(w), E, K, N, _ptr(out), _ptr(scales),
                                       flags, wp, wn, sh)
     _check(st, "gq_fp8_expert_dim1")
+    return out, scales
+
+
+def expert_rowwise(w: torch.Tensor, *, out=None, scales=None, stream=None,
+                   pow2_scales: bool = False):
+    """Stacked expert weights scaled per row: w bf16 (E, N, K) CUDA tensor,
+    K % 8 == 0; one scale per (expert, row), the amax over the row's K
+    elements.  Returns (q float8_e4m3fn (E, N, K), scales float32 (E, N))."""
+    if not (isinstance(w, torch.Tensor) and w.is_cuda and w.dtype == torch.bfloat16
+            and w.dim() == 3 and w.is_contiguous()):
+        raise ValueError("expert_rowwise: w must be a contiguous 3-D bf16 CUDA tensor")
+    E, N, K = w.shape
+    dev = w.device
+    if out is None:
+        out = torch.empty((E, N, K), dtype=torch.float8_e4m3fn, device=dev)
+    if scales is None:
+        scales = torch.empty((E, N), dtype=torch.float32, device=dev)
+    if out.shape != (E, N, K) or out.element_size() != 1 or not out.is_contiguous():
+        raise ValueError("expert_rowwise: out must be a contiguous 1-byte (E, N, K) tensor")
+    if scales.shape != (E, N) or scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError("expert_rowwise: scales must be a contiguous float32 (E, N) tensor")
+    sh = _stream_handle(stream, dev)
+    flags = GQ_SCALE_POW2 if pow2_scales else 0
+    with torch.cuda.device(dev):
+        st = lib().gq_fp8_expert_rowwise(_ptr(w), E, N, K, _ptr(out), _ptr(scales), flags, sh)
+    _check(st, "gq_fp8_expert_rowwise")
     return out, scales
 
 

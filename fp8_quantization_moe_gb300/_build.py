@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgqfp8.so")
 SOURCES = ["gq_api.cu", "gq_colwise.cu", "gq_rowwise.cu", "gq_noalloc.cu", "gq_mxfp8.cu",
-           "gq_wgrad.cu"]
+           "gq_wgrad.cu", "gq_rows.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", "-prec-div=true",

@@ -78,6 +78,8 @@ void setup_device(int dev) {
   st = mx::setup(info);
   if (st != GQ_OK) return;
   st = wgrad::setup(info);
+  if (st != GQ_OK) return;
+  st = rows::setup(info);
 }
 
 // Set-up for the current device (once per device per process).
@@ -314,6 +316,39 @@ gq_status gq_fp8_expert_dim1(const void* w, int64_t E, int64_t K, int64_t N, voi
   return colwise::launch(*info, g_dbg, w, static_cast<int32_t>(M), static_cast<int32_t>(N),
                          nullptr, static_cast<int32_t>(K), static_cast<int32_t>(E), out, scales,
                          flags, workspace, s);
+}
+
+gq_status gq_fp8_expert_rowwise(const void* w, int64_t E, int64_t N, int64_t K, void* out,
+                                float* scales, uint32_t flags, gq_stream_t stream) {
+  const char* name = "gq_fp8_expert_rowwise";
+  if (flags & ~static_cast<uint32_t>(GQ_SCALE_POW2))
+    return fail(GQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name,
+                flags & ~static_cast<uint32_t>(GQ_SCALE_POW2));
+  if (E < 1 || N < 0 || K < 0)
+    return fail(GQ_ERR_INVALID_ARG, "%s: bad sizes (%lld, %lld, %lld)", name,
+                static_cast<long long>(E), static_cast<long long>(N),
+                static_cast<long long>(K));
+  if (E > kMaxExtent || N > kMaxExtent || K > kMaxExtent)
+    return fail(GQ_ERR_UNSUPPORTED, "%s: extent >= 2^31", name);
+  if (K % 8 != 0)
+    return fail(GQ_ERR_UNSUPPORTED, "%s: K = %lld is not a multiple of 8", name,
+                static_cast<long long>(K));
+  const int64_t rows = E * N;  // both below 2^31: no overflow
+  if (rows == 0) return GQ_OK;
+  if (scales == nullptr || !aligned(scales, 4))
+    return fail(GQ_ERR_INVALID_ARG, "%s: scales NULL or misaligned", name);
+  if (K > 0) {
+    if (w == nullptr || out == nullptr)
+      return fail(GQ_ERR_INVALID_ARG, "%s: input or output is NULL", name);
+    if (!aligned(w, 16) || !aligned(out, 16))
+      return fail(GQ_ERR_INVALID_ARG, "%s: input and output must be 16-byte aligned", name);
+  }
+  const DeviceInfo* info = nullptr;
+  gq_status st = current_device(&info);
+  if (st != GQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_fill_empty_scales(scales, rows, flags, s);
+  return rows::launch(*info, w, rows, K, out, scales, (flags & GQ_SCALE_POW2) != 0, s);
 }
 
 gq_status gq_fp8_rowwise_t(const void* a, int64_t N, int64_t Mg,

@@ -19,6 +19,7 @@ struct DeviceInfo {
   int colwise_ctas_per_sm = 0;
   int rowwise_ctas_per_sm = 0;
   int mx_ctas_per_sm = 0;
+  int rows_ctas_per_sm = 0;
 };
 
 // Launch-time knobs (test hooks).
@@ -80,6 +81,12 @@ gq_status setup(DeviceInfo& info);
 gq_status launch(const DeviceInfo& info, const void* x, int64_t M, int64_t K, void* out,
                  uint8_t* scales, int mode, cudaStream_t stream);
 }  // namespace mx
+
+namespace rows {
+gq_status setup(DeviceInfo& info);
+gq_status launch(const DeviceInfo& info, const void* w, int64_t rows, int64_t K, void* out,
+                 float* scales, bool pow2, cudaStream_t stream);
+}  // namespace rows
 
 namespace wgrad {
 gq_status setup(DeviceInfo& info);

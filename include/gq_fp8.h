@@ -215,6 +215,25 @@ gq_status gq_fp8_expert_dim1(const void* w, int64_t E, int64_t K, int64_t N, voi
                              size_t workspace_bytes, gq_stream_t stream);
 
 /*
+ * Scaling of stacked expert weights per row: the "fp8 rowwise kernels for
+ * expert weights" of the pytorch/ao #2668 page's PR stack (#2696).  Each
+ * expert's (N, K) matrix is scaled per row, the amax taken over the row's
+ * K elements: scale[e][n] = 448 / max(amax, 1e-12) (IEEE fp32; rounded down
+ * to a power of two with GQ_SCALE_POW2), out[e][n][k] = e4m3(fp32(w[e][n][k]
+ * * scale[e][n])), round-to-nearest-even, saturating.  With K = 0 every
+ * scale is 448 / 1e-12.
+ *
+ *   w        bf16 [E, N, K] row-major, 16-byte aligned.          (input)
+ *   E, N, K  E >= 1, N >= 0, K >= 0, each below 2^31; K % 8 == 0.
+ *   out      e4m3 bytes [E, N, K] row-major, 16-byte aligned.    (output)
+ *   scales   fp32 [E, N] row-major: scale of expert e, row n.    (output)
+ *   flags    0 or GQ_SCALE_POW2.
+ *   stream   the CUDA stream to run on.  No workspace.
+ */
+gq_status gq_fp8_expert_rowwise(const void* w, int64_t E, int64_t N, int64_t K, void* out,
+                                float* scales, uint32_t flags, gq_stream_t stream);
+
+/*
  * mxfp8 cast along dim0 (pytorch/ao page "[mxfp8 moe training] fix mxfp8
  * a2a bench script; set mxfp8 a2a scaling type to RCEIL", Summary: the
  * dim0_mxfp8_floor cast benchmark and the RCEIL scaling type).  Every 32

@@ -500,6 +500,32 @@ def test_expert_dim1(gq, E, K, N, pow2):
                 f"expert_dim1_{E}x{K}x{N}")
 
 
+@pytest.mark.parametrize("E,N,K,pow2", [
+    (1, 1, 8, False), (3, 37, 40, False), (2, 129, 4096, False), (2, 65, 4104, False),
+    (1, 3, 8192, True), (8, 300, 264, False), (6, 1000, 520, True), (4, 0, 16, False),
+    (5, 7, 0, False), (5, 7, 0, True),
+])
+def test_expert_rowwise(gq, E, N, K, pow2):
+    """Stacked expert weights scaled per row, against the oracle, bit for
+    bit: rows shorter than a warp's first load, rows held in registers (up
+    to 4096 elements) and longer rows read twice, an all-zero row, many rows
+    per warp, N = 0 (nothing) and K = 0 (scales only)."""
+    rng = np.random.default_rng(620 + E + N + K)
+    x = rng.standard_normal((E, N, K)).astype(np.float32)
+    x *= np.power(np.float32(10), rng.uniform(-3, 3, size=(E, N, 1))).astype(np.float32)
+    if N > 2 and K:
+        x[E - 1, 2] = 0.0
+    w = synth.to_bf16_bits(x)
+    out = torch.full((E, N, K), SENTINEL, dtype=torch.uint8, device="cuda")
+    sc = torch.full((E, N), -1.0, dtype=torch.float32, device="cuda")
+    wd = torch.from_numpy(np.ascontiguousarray(w).view(np.int16)).view(torch.bfloat16).cuda()
+    q, s = gq.expert_rowwise(wd, out=out.view(torch.float8_e4m3fn), scales=sc, pow2_scales=pow2)
+    gq.check_device_error()
+    rq, rs = oracle.expert_rowwise(w, pow2=pow2)
+    assert_same(q.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), rq, rs,
+                f"expert_rowwise_{E}x{N}x{K}")
+
+
 @pytest.mark.parametrize("M,K,mode", [
     (1, 32, "floor"), (1, 32, "rceil"), (24, 256, "floor"), (24, 256, "rceil"),
     (333, 4096, "floor"), (333, 4096, "rceil"), (4097, 96, "rceil"), (0, 64, "floor"),

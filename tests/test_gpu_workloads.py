@@ -152,6 +152,23 @@ def test_expert_dim1_full_size(gq):
                 "expert_dim1_8x4096x4096")
 
 
+def test_expert_rowwise_full_size(gq):
+    """Eight experts of (4096, 4096) bf16 weights scaled per row -- 256 MB,
+    larger than L2 -- in full."""
+    rng = np.random.default_rng(602)
+    E, N, K = 8, 4096, 4096
+    x = rng.standard_normal((E, N, K), dtype=np.float32)
+    x *= np.power(np.float32(10), rng.uniform(-2, 2, size=(E, N, 1))).astype(np.float32)
+    w = synth.to_bf16_bits(x)
+    del x
+    wd = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).cuda()
+    q, s = gq.expert_rowwise(wd)
+    gq.check_device_error()
+    rq, rs = oracle_parallel.expert_rowwise(w)
+    assert_same(q.view(torch.uint8).cpu().numpy(), s.cpu().numpy(), rq, rs,
+                "expert_rowwise_8x4096x4096")
+
+
 @pytest.mark.parametrize("mode", ["floor", "rceil"])
 def test_mxfp8_full_size(gq, mode):
     """The colwise benchmark input X (65536, 4096) through the mxfp8 cast, in

@@ -230,3 +230,21 @@ def test_binding_rejects_bad_wgrad_and_mxfp8_args(gq):
         gq.mxfp8_dim0(torch.zeros((4, 32), dtype=torch.bfloat16))
     with pytest.raises(ValueError):   # unknown mode is checked before the device
         gq.mxfp8_dim0(torch.zeros((4, 32), dtype=torch.bfloat16), "nearest")
+
+
+@pytest.mark.parametrize("args,status", [
+    # w, E, N, K, out, scales, flags
+    ((A16, 0, 16, 16, A16, A16, 0), 1),           # no experts
+    ((A16, 2, -1, 16, A16, A16, 0), 1),           # negative N
+    ((A16, 2, 16, -8, A16, A16, 0), 1),           # negative K
+    ((A16, 2, 16, 12, A16, A16, 0), 2),           # K % 8
+    ((A16, 2, 16, 1 << 31, A16, A16, 0), 2),      # K >= 2^31
+    ((A16, 2, 16, 16, A16, A16, 2), 1),           # GQ_WORKSPACE_ZEROED: no workspace here
+    ((A16, 2, 16, 16, None, A16, 0), 1),          # NULL output
+    ((None, 2, 16, 16, A16, A16, 0), 1),          # NULL input
+    ((A16 + 8, 2, 16, 16, A16, A16, 0), 1),       # input not 16-byte aligned
+    ((A16, 2, 16, 16, A16, None, 0), 1),          # NULL scales
+    ((A16, 2, 0, 16, None, None, 0), 0),          # no rows: nothing to do
+])
+def test_expert_rowwise_host_validation(gq, args, status):
+    assert gq.lib().gq_fp8_expert_rowwise(*args, None) == status
