@@ -34,11 +34,11 @@
 // the phase-B tiles up to `limit` tiles behind it have been taken -- the
 // phase-A data in flight, and so what L2 must hold until phase B re-reads
 // it, stays bounded (`limit`: the longest strip's phase-B tile count plus
-// 2.5 slabs of phase-B tiles, or 1.25 phase-A tiles per block if that is
-// more); `limit` exceeds the longest strip's phase-B tile count, so the
-// strips of those phase-B tiles precede the item and are all claimed, and
-// the wait always ends.  Phase B waits only for strips whose phase-A tiles
-// are all claimed.  Claims are made by running blocks, in order, and each
+// 2.5 slabs of phase-B tiles, or 1.75 phase-A tiles per block where 2.5
+// slabs come to less than 1.25 of them); `limit` exceeds the longest
+// strip's phase-B tile count, so the strips of those phase-B tiles precede
+// the item and are all claimed, and the wait always ends.  Phase B waits
+// only for strips whose phase-A tiles are all claimed.  Claims are made by running blocks, in order, and each
 // block works through its claims in order, so every wait ends whichever
 // blocks are resident (the launch needs no co-residency).
 //
@@ -103,6 +103,7 @@ constexpr int kStageBytes = kRows * kRowBytes;
 constexpr int kBSplit = 2;  // phase-B tiles per phase-A tile (when they stay >= kTileStep rows)
 constexpr int kWarmSlabs = 1;  // column slabs prefetched into L2 at the start
 constexpr int kLeadQuarters = 10;  // phase-A lead: the longest strip + 2.5 slabs of phase-B tiles
+constexpr int kShortLeadEighths = 14;  // the lead where slabs are short: 1.75 phase-A tiles per block
 static_assert(kW == 128, "lane maps assume 128-column slabs");
 static_assert(kResStages <= kStages, "a resident strip fits the ring");
 static_assert(kStages % kConsA == 0 && kStages % kConsB == 0 && kStages <= 32,
@@ -291,11 +292,16 @@ __device__ __forceinline__ void build_plan(Smem& s, const Params& p, int lane) {
     // the lead: kLeadQuarters / 4 slabs of phase-B tiles, but never less
     // than about one phase-A tile per block in flight, which phase one needs
     // to keep every block busy (a slab of few tiles -- few rows, or uniform groups --
-    // would otherwise starve it)
+    // would otherwise starve it); where that floor binds, the lead is
+    // counted in tiles per block, kShortLeadEighths / 8 of them, which
+    // holds about as many bytes in L2 as 2.5 slabs of a 65536-row input
     const int64_t quarters = p.forced_lag > 0 ? 4 * static_cast<int64_t>(p.forced_lag) : kLeadQuarters;
     int64_t lead = quarters * cb / 4;
-    if (p.forced_lag <= 0)
-      lead = max(lead, (5 * static_cast<int64_t>(gridDim.x) * p.b_split) / 4);
+    if (p.forced_lag <= 0) {
+      const int64_t per_block = static_cast<int64_t>(gridDim.x) * p.b_split;
+      const int64_t floor_lead = 5 * per_block / 4;
+      if (lead < floor_lead) lead = max(floor_lead, kShortLeadEighths * per_block / 8);
+    }
     int64_t limit = static_cast<int64_t>(maxnt) + lead;
     if (limit > (int64_t(1) << 30)) limit = int64_t(1) << 30;
     s.plan.nsl = nsl;
